@@ -1,0 +1,383 @@
+/*
+ * CPU oracle for the compensated-FP32 projection — TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is the slow, plain reference that the CUDA path is checked against.
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+ * load it.  It shares no code, header, table or helper with the CUDA library and
+ * includes nothing from it.
+ *
+ * Source of the method: laya.cpp, "docs/vulkan.md" (Vulkan backend page),
+ *   - paragraph "Compensated FP32 splits each projection input into two FP16
+ *     components ..." : two FP16 components per input, both products with FP32
+ *     accumulators, combined in FP32; FP16 weights are exact;
+ *   - paragraph "Each input split and output merge uses a single GPU dispatch ..." :
+ *     round to nearest-even including subnormals, residual scaled by 1024;
+ *   - paragraph on the compensated acceptance ("The residual component uses a
+ *     scale of 1024 to avoid FP16 overflow at large activations").
+ * The merge formula y = acc_hi + acc_lo * 2^-10 is the plain reading of
+ * "combines them in FP32" with the 1024 scale undone.
+ *
+ * Every floating-point step here is done in IEEE double, where each step used is
+ * exact, and then rounded once to the target format.  Compile with
+ * -ffp-contract=off (no fused multiply-add) and without fast-math.
+ *
+ * Parity pins (tests/test_oracle_*.py): fp16_rne against brute-force nearest
+ * search over every binary16 value and against numpy's float16 cast; split
+ * against hand-derived bits and the reconstruction bound; merge against numpy
+ * float32 arithmetic and hand-derived special pairs; GEMMs against closed-form
+ * special cases, numpy float64 matmul for the true product, and the split's
+ * reconstruction bound.  No function here is unpinned.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ------------------------------------------------------------------------- */
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+/* Normal values (1 + f/1024) * 2^(E)   for E = -14 .. 15;                      */
+/* subnormal values f * 2^-24           for f = 1 .. 1023;                      */
+/* largest finite 65504 = (2 - 2^-10) * 2^15.                                   */
+/* ------------------------------------------------------------------------- */
+
+/* Round a non-negative double t (t < 2^12) to the nearest integer, ties to the
+ * even integer. */
+static double round_half_even(double t)
+{
+    double f = floor(t);
+    double d = t - f; /* exact: t < 2^12 has at most 53 significant bits */
+    if (d > 0.5)
+        return f + 1.0;
+    if (d < 0.5)
+        return f;
+    return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+/* Value of a binary16 bit pattern, exactly, as a double. */
+double oracle_fp16_value(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0x1f)
+        v = (f == 0) ? INFINITY : NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -24);
+    else
+        v = ldexp(1024.0 + (double)f, e - 25);
+    return sign ? -v : v;
+}
+
+/* binary16 roundTiesToEven of the real number v (given exactly as a double),
+ * with gradual underflow and overflow to infinity.
+ *
+ * The rounding is done on the real line: find the spacing q of binary16 values
+ * in the binade of |v| (the subnormal range shares the spacing 2^-24 of the
+ * smallest normal binade; above 65504 the spacing is continued as if the
+ * exponent range were unbounded), round |v|/q to an integer with ties to even,
+ * and scale back.  A result above 65504 is an overflow, which includes the tie
+ * at 65520 (it rounds to the even neighbour 65536 = 2^16). */
+uint16_t oracle_fp16_rne(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v))
+        return (uint16_t)(sign | 0x7e00u);
+    double a = fabs(v);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7c00u);
+
+    int e2;
+    (void)frexp(a, &e2); /* a in [2^(e2-1), 2^e2) for a > 0 */
+    int E = e2 - 1;
+    if (a == 0.0 || E < -14)
+        E = -14;
+    double q = ldexp(1.0, E - 10); /* spacing of binary16 values in this binade */
+    double r = round_half_even(a / q) * q; /* both scalings are exact */
+
+    if (r > 65504.0)
+        return (uint16_t)(sign | 0x7c00u);
+    if (r < ldexp(1.0, -14)) /* zero or subnormal: r = f * 2^-24 */
+        return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -24)));
+    (void)frexp(r, &e2);
+    E = e2 - 1; /* -14 .. 15 */
+    uint16_t f = (uint16_t)(r / ldexp(1.0, E - 10) - 1024.0);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | f);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Split and merge (one element each).                                        */
+/* ------------------------------------------------------------------------- */
+
+/* hi = fp16_rne(x); lo = fp16_rne((x - hi) * 1024), the difference and the
+ * scaling taken exactly. */
+static void split_one(float x, uint16_t* hi, uint16_t* lo)
+{
+    uint16_t h = oracle_fp16_rne((double)x);
+    double r = (double)x - oracle_fp16_value(h); /* exact in double */
+    *hi = h;
+    *lo = oracle_fp16_rne(r * 1024.0);
+}
+
+/* y = acc_hi + acc_lo * 2^-10 in binary32: the product rounded to binary32,
+ * then the sum rounded to binary32 (two separate IEEE operations, no fused
+ * multiply-add).  Each operation is done exactly in double and rounded once to
+ * float; for a single +, -, * on binary32 operands this gives the correctly
+ * rounded binary32 result. */
+static float merge_one(float acc_hi, float acc_lo)
+{
+    float t = (float)((double)acc_lo * 0x1p-10);
+    return (float)((double)acc_hi + (double)t);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Thread pool helper: run fn(lo, hi, ctx) over [0, n) in nthreads chunks.    */
+/* ------------------------------------------------------------------------- */
+
+typedef void (*range_fn)(int64_t lo, int64_t hi, void* ctx);
+
+struct range_job {
+    range_fn fn;
+    void* ctx;
+    int64_t lo, hi;
+};
+
+static void* range_thread(void* p)
+{
+    struct range_job* j = (struct range_job*)p;
+    j->fn(j->lo, j->hi, j->ctx);
+    return NULL;
+}
+
+int oracle_default_threads(void)
+{
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+static void parallel_for(int64_t n, int nthreads, range_fn fn, void* ctx)
+{
+    if (nthreads <= 0)
+        nthreads = oracle_default_threads();
+    if ((int64_t)nthreads > n)
+        nthreads = (int)(n > 0 ? n : 1);
+    if (nthreads <= 1) {
+        fn(0, n, ctx);
+        return;
+    }
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int* running = (int*)malloc(sizeof(int) * (size_t)nthreads);
+    struct range_job* jobs = (struct range_job*)malloc(sizeof(struct range_job) * (size_t)nthreads);
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].fn = fn;
+        jobs[t].ctx = ctx;
+        jobs[t].lo = n * t / nthreads;
+        jobs[t].hi = n * (t + 1) / nthreads;
+        running[t] = pthread_create(&th[t], NULL, range_thread, &jobs[t]) == 0;
+        if (!running[t])
+            fn(jobs[t].lo, jobs[t].hi, ctx); /* run inline if a thread cannot start */
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (running[t])
+            pthread_join(th[t], NULL);
+    free(jobs);
+    free(running);
+    free(th);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Elementwise entry points.                                                  */
+/* ------------------------------------------------------------------------- */
+
+struct split_ctx {
+    const float* x;
+    uint16_t* hi;
+    uint16_t* lo;
+};
+
+static void split_range(int64_t a, int64_t b, void* p)
+{
+    struct split_ctx* c = (struct split_ctx*)p;
+    for (int64_t i = a; i < b; ++i)
+        split_one(c->x[i], &c->hi[i], &c->lo[i]);
+}
+
+void oracle_split(const float* x, uint16_t* hi, uint16_t* lo, int64_t n, int nthreads)
+{
+    struct split_ctx c = {x, hi, lo};
+    parallel_for(n, nthreads, split_range, &c);
+}
+
+struct merge_ctx {
+    const float* acc_hi;
+    const float* acc_lo;
+    float* y;
+};
+
+static void merge_range(int64_t a, int64_t b, void* p)
+{
+    struct merge_ctx* c = (struct merge_ctx*)p;
+    for (int64_t i = a; i < b; ++i)
+        c->y[i] = merge_one(c->acc_hi[i], c->acc_lo[i]);
+}
+
+void oracle_merge(const float* acc_hi, const float* acc_lo, float* y, int64_t n, int nthreads)
+{
+    struct merge_ctx c = {acc_hi, acc_lo, y};
+    parallel_for(n, nthreads, merge_range, &c);
+}
+
+/* ------------------------------------------------------------------------- */
+/* GEMMs.  x: binary32 [M, K] row-major.  W: binary16 bits [N, K] row-major.   */
+/* Output element (i, j) is a dot product of row i of x with row j of W.       */
+/* If rows/cols are given, only the `count` listed elements are computed       */
+/* (out[s] for pair (rows[s], cols[s])); otherwise all M*N, out[i*N + j].      */
+/* Sums are taken in double, in increasing k.                                  */
+/* ------------------------------------------------------------------------- */
+
+enum gemm_kind { GEMM_COMP = 0, GEMM_TRUE = 1, GEMM_CAST = 2, GEMM_DEN = 3 };
+
+struct gemm_ctx {
+    enum gemm_kind kind;
+    const float* x;
+    const uint16_t* W;
+    int64_t M, N, K;
+    const int64_t* rows;
+    const int64_t* cols;
+    float* outf;
+    double* outd;
+};
+
+/* One output element.  hi_row/lo_row hold the split of row i of x (COMP and
+ * CAST kinds). */
+static double gemm_elem(const struct gemm_ctx* c, int64_t i, int64_t j, const uint16_t* hi_row,
+                        const uint16_t* lo_row)
+{
+    const float* xr = c->x + i * c->K;
+    const uint16_t* wr = c->W + j * c->K;
+    switch (c->kind) {
+    case GEMM_COMP: {
+        /* the method: acc_hi = sum hi*w, acc_lo = sum lo*w, y = acc_hi + acc_lo * 2^-10 */
+        double s_hi = 0.0, s_lo = 0.0;
+        for (int64_t k = 0; k < c->K; ++k) {
+            double w = oracle_fp16_value(wr[k]);
+            s_hi += oracle_fp16_value(hi_row[k]) * w;
+            s_lo += oracle_fp16_value(lo_row[k]) * w;
+        }
+        return s_hi + s_lo * 0x1p-10;
+    }
+    case GEMM_TRUE: {
+        double s = 0.0;
+        for (int64_t k = 0; k < c->K; ++k)
+            s += (double)xr[k] * oracle_fp16_value(wr[k]);
+        return s;
+    }
+    case GEMM_CAST: {
+        /* a single FP16 cast of x: only the hi component */
+        double s = 0.0;
+        for (int64_t k = 0; k < c->K; ++k)
+            s += oracle_fp16_value(hi_row[k]) * oracle_fp16_value(wr[k]);
+        return s;
+    }
+    case GEMM_DEN:
+    default: {
+        double s = 0.0;
+        for (int64_t k = 0; k < c->K; ++k)
+            s += fabs((double)xr[k]) * fabs(oracle_fp16_value(wr[k]));
+        return s;
+    }
+    }
+}
+
+static void gemm_store(const struct gemm_ctx* c, int64_t slot, double v)
+{
+    if (c->kind == GEMM_DEN)
+        c->outd[slot] = v;
+    else
+        c->outf[slot] = (float)v;
+}
+
+static void split_row(const struct gemm_ctx* c, int64_t i, uint16_t* hi_row, uint16_t* lo_row)
+{
+    const float* xr = c->x + i * c->K;
+    for (int64_t k = 0; k < c->K; ++k)
+        split_one(xr[k], &hi_row[k], &lo_row[k]);
+}
+
+/* Full product: a range of rows i. */
+static void gemm_rows(int64_t a, int64_t b, void* p)
+{
+    const struct gemm_ctx* c = (const struct gemm_ctx*)p;
+    size_t kk = (size_t)(c->K > 0 ? c->K : 1);
+    uint16_t* hi_row = (uint16_t*)malloc(kk * sizeof(uint16_t));
+    uint16_t* lo_row = (uint16_t*)malloc(kk * sizeof(uint16_t));
+    for (int64_t i = a; i < b; ++i) {
+        split_row(c, i, hi_row, lo_row);
+        for (int64_t j = 0; j < c->N; ++j)
+            gemm_store(c, i * c->N + j, gemm_elem(c, i, j, hi_row, lo_row));
+    }
+    free(hi_row);
+    free(lo_row);
+}
+
+/* Sampled product: a range of listed (row, col) pairs. */
+static void gemm_pairs(int64_t a, int64_t b, void* p)
+{
+    const struct gemm_ctx* c = (const struct gemm_ctx*)p;
+    size_t kk = (size_t)(c->K > 0 ? c->K : 1);
+    uint16_t* hi_row = (uint16_t*)malloc(kk * sizeof(uint16_t));
+    uint16_t* lo_row = (uint16_t*)malloc(kk * sizeof(uint16_t));
+    int64_t have = -1;
+    for (int64_t s = a; s < b; ++s) {
+        int64_t i = c->rows[s], j = c->cols[s];
+        if (i != have) {
+            split_row(c, i, hi_row, lo_row);
+            have = i;
+        }
+        gemm_store(c, s, gemm_elem(c, i, j, hi_row, lo_row));
+    }
+    free(hi_row);
+    free(lo_row);
+}
+
+static void gemm_run(enum gemm_kind kind, const float* x, const uint16_t* W, int64_t M, int64_t N,
+                     int64_t K, const int64_t* rows, const int64_t* cols, int64_t count, float* outf,
+                     double* outd, int nthreads)
+{
+    struct gemm_ctx c = {kind, x, W, M, N, K, rows, cols, outf, outd};
+    if (rows && cols)
+        parallel_for(count, nthreads, gemm_pairs, &c);
+    else
+        parallel_for(M, nthreads, gemm_rows, &c);
+}
+
+/* The compensated product, following the method step by step (the gate
+ * oracle): y = fp32( sum_k hi_ik w_jk + 2^-10 * sum_k lo_ik w_jk ). */
+void oracle_gemm_comp(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K,
+                      const int64_t* rows, const int64_t* cols, int64_t count, float* y, int nthreads)
+{
+    gemm_run(GEMM_COMP, x, W, M, N, K, rows, cols, count, y, NULL, nthreads);
+}
+
+/* The true product of the FP32 input: y = fp32( sum_k x_ik w_jk ). */
+void oracle_gemm_true(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K,
+                      const int64_t* rows, const int64_t* cols, int64_t count, float* y, int nthreads)
+{
+    gemm_run(GEMM_TRUE, x, W, M, N, K, rows, cols, count, y, NULL, nthreads);
+}
+
+/* A single FP16 cast of x (the best such a cast can do): y = fp32( sum_k fp16(x_ik) w_jk ). */
+void oracle_gemm_cast(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K,
+                      const int64_t* rows, const int64_t* cols, int64_t count, float* y, int nthreads)
+{
+    gemm_run(GEMM_CAST, x, W, M, N, K, rows, cols, count, y, NULL, nthreads);
+}
+
+/* The error scale of a dot product: den = sum_k |x_ik| |w_jk| (double). */
+void oracle_gemm_den(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K,
+                     const int64_t* rows, const int64_t* cols, int64_t count, double* den, int nthreads)
+{
+    gemm_run(GEMM_DEN, x, W, M, N, K, rows, cols, count, NULL, den, nthreads);
+}
