@@ -52,7 +52,7 @@ static double round_half_even(double t)
         return f + 1.0;
     if (d < 0.5)
         return f;
-    return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+    return (((int64_t)f & 1) == 0) ? f : f + 1.0;
 }
 
 /* Value of a binary16 bit pattern, exactly, as a double. */
@@ -74,12 +74,12 @@ double oracle_fp16_value(uint16_t h)
 /* binary16 roundTiesToEven of the real number v (given exactly as a double),
  * with gradual underflow and overflow to infinity.
  *
- * The rounding is done on the real line: find the spacing q of binary16 values
- * in the binade of |v| (the subnormal range shares the spacing 2^-24 of the
- * smallest normal binade; above 65504 the spacing is continued as if the
- * exponent range were unbounded), round |v|/q to an integer with ties to even,
- * and scale back.  A result above 65504 is an overflow, which includes the tie
- * at 65520 (it rounds to the even neighbour 65536 = 2^16). */
+ * The rounding is done on the real line: |v| lies in the binade [2^E, 2^(E+1));
+ * binary16 values there are n * 2^(E-10) for integers n in [1024, 2048) (the
+ * subnormal range, |v| < 2^-14, shares the spacing 2^-24 of the smallest normal
+ * binade, with n < 1024).  So n = round_half_even(|v| / 2^(E-10)), an exact
+ * scaling.  n = 2048 carries into the next binade; a result above 65504
+ * (E = 15, n = 2048) is an overflow, which includes the tie at 65520. */
 uint16_t oracle_fp16_rne(double v)
 {
     uint16_t sign = signbit(v) ? 0x8000u : 0u;
@@ -89,22 +89,22 @@ uint16_t oracle_fp16_rne(double v)
     if (isinf(a))
         return (uint16_t)(sign | 0x7c00u);
 
-    int e2;
-    (void)frexp(a, &e2); /* a in [2^(e2-1), 2^e2) for a > 0 */
+    int e2 = 0;
+    if (a != 0.0)
+        (void)frexp(a, &e2); /* a in [2^(e2-1), 2^e2) */
     int E = e2 - 1;
     if (a == 0.0 || E < -14)
         E = -14;
-    double q = ldexp(1.0, E - 10); /* spacing of binary16 values in this binade */
-    double r = round_half_even(a / q) * q; /* both scalings are exact */
-
-    if (r > 65504.0)
-        return (uint16_t)(sign | 0x7c00u);
-    if (r < ldexp(1.0, -14)) /* zero or subnormal: r = f * 2^-24 */
-        return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -24)));
-    (void)frexp(r, &e2);
-    E = e2 - 1; /* -14 .. 15 */
-    uint16_t f = (uint16_t)(r / ldexp(1.0, E - 10) - 1024.0);
-    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | f);
+    int n = (int)round_half_even(ldexp(a, 10 - E)); /* a / 2^(E-10), exact */
+    if (n == 2048) {                                  /* carried into the next binade */
+        n = 1024;
+        E += 1;
+    }
+    if (E > 15)
+        return (uint16_t)(sign | 0x7c00u); /* above 65504: overflow to infinity */
+    if (n < 1024)                           /* E == -14: zero or subnormal, value n * 2^-24 */
+        return (uint16_t)(sign | (uint16_t)n);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(n - 1024));
 }
 
 /* ------------------------------------------------------------------------- */
@@ -248,44 +248,52 @@ struct gemm_ctx {
     const int64_t* cols;
     float* outf;
     double* outd;
+    const double* wd; /* W decoded to double, [N, K], or NULL (decode per use) */
 };
 
-/* One output element.  hi_row/lo_row hold the split of row i of x (COMP and
- * CAST kinds). */
-static double gemm_elem(const struct gemm_ctx* c, int64_t i, int64_t j, const uint16_t* hi_row,
-                        const uint16_t* lo_row)
+/* Row i of x as the doubles the kind needs: x itself (TRUE, DEN) or its split
+ * components hi, lo (COMP, CAST). */
+static void prepare_row(const struct gemm_ctx* c, int64_t i, double* a, double* b)
 {
     const float* xr = c->x + i * c->K;
-    const uint16_t* wr = c->W + j * c->K;
+    for (int64_t k = 0; k < c->K; ++k) {
+        if (c->kind == GEMM_TRUE || c->kind == GEMM_DEN) {
+            a[k] = (double)xr[k];
+            b[k] = 0.0;
+        } else {
+            uint16_t h, l;
+            split_one(xr[k], &h, &l);
+            a[k] = oracle_fp16_value(h);
+            b[k] = oracle_fp16_value(l);
+        }
+    }
+}
+
+/* One output element from the prepared row (a, b) and row w of W (doubles). */
+static double gemm_elem(const struct gemm_ctx* c, const double* a, const double* b, const double* w)
+{
     switch (c->kind) {
     case GEMM_COMP: {
         /* the method: acc_hi = sum hi*w, acc_lo = sum lo*w, y = acc_hi + acc_lo * 2^-10 */
         double s_hi = 0.0, s_lo = 0.0;
         for (int64_t k = 0; k < c->K; ++k) {
-            double w = oracle_fp16_value(wr[k]);
-            s_hi += oracle_fp16_value(hi_row[k]) * w;
-            s_lo += oracle_fp16_value(lo_row[k]) * w;
+            s_hi += a[k] * w[k];
+            s_lo += b[k] * w[k];
         }
         return s_hi + s_lo * 0x1p-10;
     }
-    case GEMM_TRUE: {
+    case GEMM_TRUE:
+    case GEMM_CAST: { /* CAST: a single FP16 cast of x, only the hi component */
         double s = 0.0;
         for (int64_t k = 0; k < c->K; ++k)
-            s += (double)xr[k] * oracle_fp16_value(wr[k]);
-        return s;
-    }
-    case GEMM_CAST: {
-        /* a single FP16 cast of x: only the hi component */
-        double s = 0.0;
-        for (int64_t k = 0; k < c->K; ++k)
-            s += oracle_fp16_value(hi_row[k]) * oracle_fp16_value(wr[k]);
+            s += a[k] * w[k];
         return s;
     }
     case GEMM_DEN:
     default: {
         double s = 0.0;
         for (int64_t k = 0; k < c->K; ++k)
-            s += fabs((double)xr[k]) * fabs(oracle_fp16_value(wr[k]));
+            s += fabs(a[k]) * fabs(w[k]);
         return s;
     }
     }
@@ -299,58 +307,85 @@ static void gemm_store(const struct gemm_ctx* c, int64_t slot, double v)
         c->outf[slot] = (float)v;
 }
 
-static void split_row(const struct gemm_ctx* c, int64_t i, uint16_t* hi_row, uint16_t* lo_row)
+static const double* w_row(const struct gemm_ctx* c, int64_t j, double* scratch)
 {
-    const float* xr = c->x + i * c->K;
+    if (c->wd)
+        return c->wd + j * c->K;
     for (int64_t k = 0; k < c->K; ++k)
-        split_one(xr[k], &hi_row[k], &lo_row[k]);
+        scratch[k] = oracle_fp16_value(c->W[j * c->K + k]);
+    return scratch;
 }
 
 /* Full product: a range of rows i. */
-static void gemm_rows(int64_t a, int64_t b, void* p)
+static void gemm_rows(int64_t lo_i, int64_t hi_i, void* p)
 {
     const struct gemm_ctx* c = (const struct gemm_ctx*)p;
     size_t kk = (size_t)(c->K > 0 ? c->K : 1);
-    uint16_t* hi_row = (uint16_t*)malloc(kk * sizeof(uint16_t));
-    uint16_t* lo_row = (uint16_t*)malloc(kk * sizeof(uint16_t));
-    for (int64_t i = a; i < b; ++i) {
-        split_row(c, i, hi_row, lo_row);
+    double* a = (double*)malloc(kk * sizeof(double));
+    double* b = (double*)malloc(kk * sizeof(double));
+    double* wsc = (double*)malloc(kk * sizeof(double));
+    for (int64_t i = lo_i; i < hi_i; ++i) {
+        prepare_row(c, i, a, b);
         for (int64_t j = 0; j < c->N; ++j)
-            gemm_store(c, i * c->N + j, gemm_elem(c, i, j, hi_row, lo_row));
+            gemm_store(c, i * c->N + j, gemm_elem(c, a, b, w_row(c, j, wsc)));
     }
-    free(hi_row);
-    free(lo_row);
+    free(a);
+    free(b);
+    free(wsc);
 }
 
 /* Sampled product: a range of listed (row, col) pairs. */
-static void gemm_pairs(int64_t a, int64_t b, void* p)
+static void gemm_pairs(int64_t lo_s, int64_t hi_s, void* p)
 {
     const struct gemm_ctx* c = (const struct gemm_ctx*)p;
     size_t kk = (size_t)(c->K > 0 ? c->K : 1);
-    uint16_t* hi_row = (uint16_t*)malloc(kk * sizeof(uint16_t));
-    uint16_t* lo_row = (uint16_t*)malloc(kk * sizeof(uint16_t));
+    double* a = (double*)malloc(kk * sizeof(double));
+    double* b = (double*)malloc(kk * sizeof(double));
+    double* wsc = (double*)malloc(kk * sizeof(double));
     int64_t have = -1;
-    for (int64_t s = a; s < b; ++s) {
+    for (int64_t s = lo_s; s < hi_s; ++s) {
         int64_t i = c->rows[s], j = c->cols[s];
         if (i != have) {
-            split_row(c, i, hi_row, lo_row);
+            prepare_row(c, i, a, b);
             have = i;
         }
-        gemm_store(c, s, gemm_elem(c, i, j, hi_row, lo_row));
+        gemm_store(c, s, gemm_elem(c, a, b, w_row(c, j, wsc)));
     }
-    free(hi_row);
-    free(lo_row);
+    free(a);
+    free(b);
+    free(wsc);
 }
 
-static void gemm_run(enum gemm_kind kind, const float* x, const uint16_t* W, int64_t M, int64_t N,
-                     int64_t K, const int64_t* rows, const int64_t* cols, int64_t count, float* outf,
-                     double* outd, int nthreads)
+struct decode_ctx {
+    const uint16_t* W;
+    double* wd;
+};
+
+static void decode_range(int64_t a, int64_t b, void* p)
 {
-    struct gemm_ctx c = {kind, x, W, M, N, K, rows, cols, outf, outd};
-    if (rows && cols)
+    struct decode_ctx* d = (struct decode_ctx*)p;
+    for (int64_t i = a; i < b; ++i)
+        d->wd[i] = oracle_fp16_value(d->W[i]);
+}
+
+static void gemm_run(enum gemm_kind kind, const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K,
+                     const int64_t* rows, const int64_t* cols, int64_t count, float* outf, double* outd,
+                     int nthreads)
+{
+    struct gemm_ctx c = {kind, x, W, M, N, K, rows, cols, outf, outd, NULL};
+    if (rows && cols) {
         parallel_for(count, nthreads, gemm_pairs, &c);
-    else
-        parallel_for(M, nthreads, gemm_rows, &c);
+        return;
+    }
+    /* full product: decode W once (falls back to per-row decoding without memory) */
+    double* wd = (double*)malloc((size_t)(N * K > 0 ? N * K : 1) * sizeof(double));
+    if (wd) {
+        struct decode_ctx d = {W, wd};
+        parallel_for(N * K, nthreads, decode_range, &d);
+        c.wd = wd;
+    }
+    parallel_for(M, nthreads, gemm_rows, &c);
+    free(wd);
 }
 
 /* The compensated product, following the method step by step (the gate
