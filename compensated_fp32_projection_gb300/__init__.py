@@ -1,0 +1,118 @@
+"""Compensated-FP32 projection for GB300 (sm_103a).
+
+The method (laya.cpp, docs/vulkan.md, compensated-FP32 paragraph): each FP32
+input x is split into hi = fp16_rne(x) and lo = fp16_rne((x - hi) * 1024), both
+are multiplied by the exact FP16 weights with FP32 accumulators, and the results
+are merged in FP32 as y = acc_hi + acc_lo * 2^-10.
+
+The torch-facing calls below carry the C ABI's names and only marshal
+arguments (device pointers, sizes, the current CUDA stream) into
+``libcompfp32.so``; every step runs in its CUDA kernels.  Outputs that are not
+given are allocated with ``torch.empty`` on the input's device.
+"""
+from __future__ import annotations
+
+from . import _native
+from ._native import CompError, device_status, status_string
+
+__all__ = [
+    "CompError",
+    "comp_split_f32",
+    "comp_merge_f32",
+    "comp_gemm_f32x16",
+    "comp_gemm_f32x16_variant",
+    "comp_gemm_f32_simt",
+    "device_status",
+    "status_string",
+]
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream(t, stream):
+    if stream is not None:
+        return int(stream) if isinstance(stream, int) else stream.cuda_stream
+    return _torch().cuda.current_stream(t.device).cuda_stream
+
+
+def _check(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def comp_split_f32(x, hi=None, lo=None, stream=None):
+    """(hi, lo) float16 tensors shaped like x: hi = fp16_rne(x), lo = fp16_rne((x-hi)*1024)."""
+    torch = _torch()
+    _check(x, torch.float32, "x")
+    hi = torch.empty(x.shape, dtype=torch.float16, device=x.device) if hi is None else hi
+    lo = torch.empty(x.shape, dtype=torch.float16, device=x.device) if lo is None else lo
+    _check(hi, torch.float16, "hi")
+    _check(lo, torch.float16, "lo")
+    if hi.numel() != x.numel() or lo.numel() != x.numel():
+        raise ValueError("hi and lo must have as many elements as x")
+    _native.call("comp_split_f32", x.data_ptr(), hi.data_ptr(), lo.data_ptr(), x.numel(), _stream(x, stream))
+    return hi, lo
+
+
+def comp_merge_f32(acc_hi, acc_lo, y=None, stream=None):
+    """y = acc_hi + acc_lo * 2^-10 (float32, two rounded operations)."""
+    torch = _torch()
+    _check(acc_hi, torch.float32, "acc_hi")
+    _check(acc_lo, torch.float32, "acc_lo")
+    if acc_hi.numel() != acc_lo.numel():
+        raise ValueError("acc_hi and acc_lo differ in size")
+    y = torch.empty(acc_hi.shape, dtype=torch.float32, device=acc_hi.device) if y is None else y
+    _check(y, torch.float32, "y")
+    if y.numel() != acc_hi.numel():
+        raise ValueError("y must have as many elements as acc_hi")
+    _native.call("comp_merge_f32", acc_hi.data_ptr(), acc_lo.data_ptr(), y.data_ptr(), acc_hi.numel(),
+                 _stream(acc_hi, stream))
+    return y
+
+
+def _gemm_args(x, W, y):
+    torch = _torch()
+    _check(x, torch.float32, "x")
+    _check(W, torch.float16, "W")
+    if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[1]:
+        raise ValueError("x must be [M, K] and W [N, K]")
+    M, K = x.shape
+    N = W.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
+    _check(y, torch.float32, "y")
+    if tuple(y.shape) != (M, N):
+        raise ValueError("y must be [M, N]")
+    return M, N, K, y
+
+
+def comp_gemm_f32x16(x, W, y=None, stream=None):
+    """The fused compensated projection y = x W^T (FP32 in, FP16 weights, FP32 out)."""
+    M, N, K, y = _gemm_args(x, W, y)
+    _native.call("comp_gemm_f32x16", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K, _stream(x, stream))
+    return y
+
+
+def comp_gemm_f32x16_variant(x, W, variant, y=None, stream=None):
+    """comp_gemm_f32x16 with a chosen kernel path (0 auto, 1 TMA loads, 2 plain loads)."""
+    M, N, K, y = _gemm_args(x, W, y)
+    _native.call("comp_gemm_f32x16_variant", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K, int(variant),
+                 _stream(x, stream))
+    return y
+
+
+def comp_gemm_f32_simt(x, W, y=None, stream=None):
+    """The true-FP32 reference product on the CUDA cores: y = x float(W)^T."""
+    M, N, K, y = _gemm_args(x, W, y)
+    _native.call("comp_gemm_f32_simt", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K, _stream(x, stream))
+    return y

@@ -1,0 +1,210 @@
+// The C ABI entry points (include/compfp32.h): argument validation, the device
+// check, and dispatch to the kernels' launchers.  Nothing here allocates
+// device memory or synchronises, except comp_device_status.
+#include <atomic>
+#include <cstring>
+
+#include "internal.h"
+
+namespace compfp32 {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// 0 = unknown, 1 = supported, 2 = unsupported; SM count alongside.
+std::atomic<int> g_dev_state[kMaxDevices];
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out)
+{
+    if (a < 0 || b < 0)
+        return false;
+    if (a != 0 && b > INT64_MAX / a)
+        return false;
+    *out = a * b;
+    return true;
+}
+
+// Byte ranges [a, a+na) and [b, b+nb) overlap.
+bool overlap(const void* a, int64_t na, const void* b, int64_t nb)
+{
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && pa < pb + static_cast<uintptr_t>(nb) && pb < pa + static_cast<uintptr_t>(na);
+}
+
+}  // namespace
+
+comp_status_t current_device(DeviceInfo* info)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return COMP_ERR_UNSUPPORTED_DEVICE;
+    }
+    int state = g_dev_state[dev].load(std::memory_order_acquire);
+    if (state == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return COMP_ERR_UNSUPPORTED_DEVICE;
+        }
+        g_dev_sms[dev].store(sms, std::memory_order_relaxed);
+        state = (major == 10 && minor == 3) ? 1 : 2;
+        g_dev_state[dev].store(state, std::memory_order_release);
+    }
+    if (state != 1)
+        return COMP_ERR_UNSUPPORTED_DEVICE;
+    info->device = dev;
+    info->sm_count = g_dev_sms[dev].load(std::memory_order_relaxed);
+    return COMP_OK;
+}
+
+namespace {
+
+// Shared checks of the two GEMM entry points.  Sets *empty when there is
+// nothing to launch (after writing y = 0 for K == 0).
+comp_status_t check_gemm(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t stream, DeviceInfo* dev, bool* empty)
+{
+    *empty = false;
+    int64_t mk, nk, mn;
+    if (M < 0 || N < 0 || K < 0 || !mul_ok(M, K, &mk) || !mul_ok(N, K, &nk) || !mul_ok(M, N, &mn))
+        return COMP_ERR_INVALID_VALUE;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return COMP_ERR_INVALID_VALUE;
+    if (mk > INT64_MAX / 4 || nk > INT64_MAX / 2 || mn > INT64_MAX / 4)
+        return COMP_ERR_INVALID_VALUE;
+    if (mn == 0) {
+        *empty = true;
+        return COMP_OK;
+    }
+    if (!y || (K > 0 && (!x || !W)))
+        return COMP_ERR_INVALID_VALUE;
+    if (overlap(y, 4 * mn, x, 4 * mk) || overlap(y, 4 * mn, W, 2 * nk))
+        return COMP_ERR_INVALID_VALUE;
+    const comp_status_t st = current_device(dev);
+    if (st != COMP_OK)
+        return st;
+    if (K == 0) {
+        *empty = true;
+        return cudaMemsetAsync(y, 0, static_cast<size_t>(4 * mn), stream) == cudaSuccess ? COMP_OK : COMP_ERR_CUDA;
+    }
+    return COMP_OK;
+}
+
+}  // namespace
+}  // namespace compfp32
+
+using namespace compfp32;
+
+extern "C" {
+
+comp_status_t comp_split_f32(const float* x, uint16_t* hi, uint16_t* lo, int64_t n, comp_stream_t stream)
+{
+    if (n < 0 || n > INT64_MAX / 4)
+        return COMP_ERR_INVALID_VALUE;
+    if (n == 0)
+        return COMP_OK;
+    if (!x || !hi || !lo)
+        return COMP_ERR_INVALID_VALUE;
+    if (overlap(x, 4 * n, hi, 2 * n) || overlap(x, 4 * n, lo, 2 * n) || overlap(hi, 2 * n, lo, 2 * n))
+        return COMP_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    const comp_status_t st = current_device(&dev);
+    if (st != COMP_OK)
+        return st;
+    return launch_split(x, hi, lo, n, dev, static_cast<cudaStream_t>(stream));
+}
+
+comp_status_t comp_merge_f32(const float* acc_hi, const float* acc_lo, float* y, int64_t n, comp_stream_t stream)
+{
+    if (n < 0 || n > INT64_MAX / 4)
+        return COMP_ERR_INVALID_VALUE;
+    if (n == 0)
+        return COMP_OK;
+    if (!acc_hi || !acc_lo || !y)
+        return COMP_ERR_INVALID_VALUE;
+    if ((y != acc_hi && overlap(y, 4 * n, acc_hi, 4 * n)) || (y != acc_lo && overlap(y, 4 * n, acc_lo, 4 * n)))
+        return COMP_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    const comp_status_t st = current_device(&dev);
+    if (st != COMP_OK)
+        return st;
+    return launch_merge(acc_hi, acc_lo, y, n, dev, static_cast<cudaStream_t>(stream));
+}
+
+comp_status_t comp_gemm_f32x16_variant(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                                       int variant, comp_stream_t stream)
+{
+    if (variant < 0 || variant > 2)
+        return COMP_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    bool empty;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const comp_status_t st = check_gemm(x, W, y, M, N, K, s, &dev, &empty);
+    if (st != COMP_OK || empty)
+        return st;
+    return launch_gemm_tc(x, W, y, M, N, K, variant, dev, s);
+}
+
+comp_status_t comp_gemm_f32x16(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                               comp_stream_t stream)
+{
+    return comp_gemm_f32x16_variant(x, W, y, M, N, K, 0, stream);
+}
+
+comp_status_t comp_gemm_f32_simt(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                                 comp_stream_t stream)
+{
+    DeviceInfo dev;
+    bool empty;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const comp_status_t st = check_gemm(x, W, y, M, N, K, s, &dev, &empty);
+    if (st != COMP_OK || empty)
+        return st;
+    return launch_gemm_simt(x, W, y, M, N, K, dev, s);
+}
+
+comp_status_t comp_device_status(comp_stream_t stream, uint32_t* where)
+{
+    if (where)
+        *where = 0;
+    DeviceInfo dev;
+    const comp_status_t st = current_device(&dev);
+    if (st != COMP_OK)
+        return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return COMP_ERR_CUDA;
+    }
+    return read_and_clear_fault(s, where);
+}
+
+const char* comp_status_string(comp_status_t status)
+{
+    switch (status) {
+    case COMP_OK:
+        return "COMP_OK";
+    case COMP_ERR_INVALID_VALUE:
+        return "COMP_ERR_INVALID_VALUE: bad pointer, size or aliasing";
+    case COMP_ERR_UNSUPPORTED_DEVICE:
+        return "COMP_ERR_UNSUPPORTED_DEVICE: the current device is not an sm_103 GPU";
+    case COMP_ERR_LAUNCH:
+        return "COMP_ERR_LAUNCH: kernel launch failed";
+    case COMP_ERR_TIMEOUT:
+        return "COMP_ERR_TIMEOUT: a kernel gave up a bounded wait";
+    case COMP_ERR_CUDA:
+        return "COMP_ERR_CUDA: a CUDA runtime call failed";
+    }
+    return "unknown comp_status_t";
+}
+
+int comp_version(void)
+{
+    return 100;  // 0.1.0
+}
+
+}  // extern "C"

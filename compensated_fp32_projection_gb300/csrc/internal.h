@@ -1,0 +1,40 @@
+// Internal declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "compfp32.h"
+
+namespace compfp32 {
+
+// Properties of the current device, checked once per device.
+struct DeviceInfo {
+    int device;
+    int sm_count;
+};
+
+// COMP_OK and fills `info` if the current device is compute capability 10.3.
+comp_status_t current_device(DeviceInfo* info);
+
+// Launchers (arguments already validated; sizes > 0).
+comp_status_t launch_split(const float* x, uint16_t* hi, uint16_t* lo, int64_t n, const DeviceInfo& dev,
+                           cudaStream_t stream);
+comp_status_t launch_merge(const float* acc_hi, const float* acc_lo, float* y, int64_t n, const DeviceInfo& dev,
+                           cudaStream_t stream);
+comp_status_t launch_gemm_simt(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                               const DeviceInfo& dev, cudaStream_t stream);
+// variant: 0 automatic, 1 TMA loads, 2 plain loads.
+comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                             int variant, const DeviceInfo& dev, cudaStream_t stream);
+
+// Reads and clears the fault word of the tensor-core kernels (after the stream
+// has been synchronised).
+comp_status_t read_and_clear_fault(cudaStream_t stream, uint32_t* where);
+
+inline comp_status_t launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? COMP_OK : COMP_ERR_LAUNCH;
+}
+
+}  // namespace compfp32

@@ -1,0 +1,150 @@
+/*
+ * compfp32.h — C ABI of the GB300 (sm_103a) compensated-FP32 projection library.
+ *
+ * The method is the "compensated FP32" projection of laya.cpp's Vulkan backend
+ * page (docs/vulkan.md):
+ *   - paragraph "Compensated FP32 splits each projection input into two FP16
+ *     components ...": every FP32 activation x is split into two FP16 values,
+ *     both are multiplied by the FP16 weights (which are stored exactly) with
+ *     FP32 accumulators, and the two results are combined in FP32;
+ *   - paragraph "Each input split and output merge uses a single GPU dispatch":
+ *     the split rounds to nearest-even, including subnormals, and scales the
+ *     residual by 1024;
+ *   - paragraph "A build-time extension of the pinned Vulkan backend supplies
+ *     true FP32 matrix kernels": a plain FP32 matrix product that never converts
+ *     its FP32 operand to FP16;
+ *   - paragraph "The fused split/merge build": split and merge fused into the
+ *     projection.
+ * In formulas, with fp16_rne the IEEE 754 binary32 -> binary16 conversion
+ * (round to nearest, ties to even, gradual underflow, overflow to infinity):
+ *     hi = fp16_rne(x)                 lo = fp16_rne((x - hi) * 1024)
+ *     acc_hi = sum_k hi[m,k] * W[n,k]  acc_lo = sum_k lo[m,k] * W[n,k]   (FP32)
+ *     y = acc_hi + acc_lo * 2^-10      (binary32 multiply, then binary32 add)
+ *
+ * Conventions shared by every call
+ *   - Binary16 values travel as uint16_t bit patterns, so this header needs no
+ *     CUDA half-precision header.
+ *   - Every pointer is DEVICE memory owned by the caller (for example a PyTorch
+ *     tensor's data pointer) on the current CUDA device.  The library keeps no
+ *     pointer after a call returns, and allocates no device memory.
+ *   - Matrices are dense and row-major: x is [M, K] (K contiguous), W is [N, K]
+ *     (K contiguous), y is [M, N] (N contiguous).  Any element-aligned address
+ *     and any size are accepted; addresses or sizes that the fast paths cannot
+ *     use (for example K not a multiple of 8) take a slower path and still
+ *     return COMP_OK.
+ *   - `stream` is a cudaStream_t (CUstream) of the current device; NULL is the
+ *     legacy default stream.  Every call only enqueues work on `stream` and never
+ *     synchronises; errors found while the kernels run are reported later (see
+ *     comp_device_status).
+ *   - Argument errors are detected before anything is enqueued and return
+ *     COMP_ERR_INVALID_VALUE.  A device that is not compute capability 10.3
+ *     returns COMP_ERR_UNSUPPORTED_DEVICE.  There is no CPU fallback (as on the
+ *     laya.cpp page: "An unavailable backend produces an error; there is no
+ *     automatic CPU fallback").
+ *   - Sizes of zero are valid no-ops, except that a GEMM with K == 0 and
+ *     M*N > 0 writes y = +0.
+ */
+#ifndef COMPFP32_H
+#define COMPFP32_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum comp_status {
+    COMP_OK = 0,
+    COMP_ERR_INVALID_VALUE = 1,      /* bad pointer, size or aliasing; nothing was enqueued */
+    COMP_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not sm_103 (GB300), or no device */
+    COMP_ERR_LAUNCH = 3,             /* the kernel launch itself failed */
+    COMP_ERR_TIMEOUT = 4,            /* a kernel gave up a bounded wait (see comp_device_status) */
+    COMP_ERR_CUDA = 5                /* another CUDA runtime call failed */
+} comp_status_t;
+
+/* An opaque cudaStream_t. */
+typedef void* comp_stream_t;
+
+/*
+ * comp_split_f32 — the split (laya.cpp docs/vulkan.md, split/merge paragraph).
+ *   x  : n binary32 values (input).
+ *   hi : n binary16 values, hi[i] = fp16_rne(x[i]) (output).
+ *   lo : n binary16 values, lo[i] = fp16_rne((x[i] - hi[i]) * 1024) (output).
+ * The two outputs are separate planes with the same indexing as x.  For every
+ * finite |x| < 65520, x - hi and its scaling are exact in binary32 and
+ * |lo| <= 16384.  |x| >= 65520 gives hi = +-inf and lo = -+inf; NaN gives NaN
+ * in both.  No value is flushed to zero.
+ * Errors: COMP_ERR_INVALID_VALUE if n < 0, a pointer is NULL while n > 0, or an
+ * output overlaps x or the other output.
+ */
+comp_status_t comp_split_f32(const float* x, uint16_t* hi, uint16_t* lo, int64_t n, comp_stream_t stream);
+
+/*
+ * comp_merge_f32 — the merge (laya.cpp docs/vulkan.md, compensated-FP32
+ * paragraph, "combines them in FP32").
+ *   acc_hi, acc_lo : n binary32 accumulators (input).
+ *   y              : n binary32 values, y[i] = rn(acc_hi[i] + rn(acc_lo[i] * 2^-10))
+ *                    (output; two rounded operations, never a fused multiply-add).
+ * y may be exactly acc_hi or exactly acc_lo (in place); any other overlap is
+ * COMP_ERR_INVALID_VALUE, as are n < 0 and a NULL pointer with n > 0.
+ */
+comp_status_t comp_merge_f32(const float* acc_hi, const float* acc_lo, float* y, int64_t n, comp_stream_t stream);
+
+/*
+ * comp_gemm_f32x16 — the fused compensated projection (laya.cpp docs/vulkan.md,
+ * compensated-FP32 paragraph and "The fused split/merge build" paragraph):
+ *   y[m,n] = acc_hi[m,n] + acc_lo[m,n] * 2^-10, with acc_hi, acc_lo the FP32
+ *   tensor-core accumulations of hi(x)·W^T and lo(x)·W^T.
+ *   x : [M, K] binary32 (input).   W : [N, K] binary16 (input).   y : [M, N] binary32 (output).
+ * One kernel: x is split on the fly in shared memory, both products accumulate
+ * in tensor memory, and the merge is the epilogue.  The accumulation order of
+ * the tensor cores is not specified; results agree with an FP64 evaluation of
+ * the same formula to within 4e-6 * sum_k |x[m,k]| |W[n,k]| per element.
+ * Errors: COMP_ERR_INVALID_VALUE if a size is negative, M*K, N*K or M*N
+ * overflows int64, a needed pointer is NULL, or y overlaps x or W.
+ */
+comp_status_t comp_gemm_f32x16(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                               comp_stream_t stream);
+
+/*
+ * comp_gemm_f32_simt — the true-FP32 reference product (laya.cpp docs/vulkan.md,
+ * paragraph on the true FP32 matrix kernels): y = x · float(W)^T with binary32
+ * fused multiply-adds on the CUDA cores; W is widened to binary32 exactly and x
+ * is never converted to FP16.  Same arguments, layouts and errors as
+ * comp_gemm_f32x16.
+ */
+comp_status_t comp_gemm_f32_simt(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                                 comp_stream_t stream);
+
+/*
+ * comp_gemm_f32x16_variant — comp_gemm_f32x16 with the kernel path chosen by
+ * the caller, for testing and measurement (the paths compute the same formula):
+ *   0 = automatic (what comp_gemm_f32x16 does),
+ *   1 = tiled tensor-memory-accelerator loads of x and W (needs 16-byte aligned
+ *       x and W and K % 8 == 0, else COMP_ERR_INVALID_VALUE),
+ *   2 = plain coalesced loads (any alignment and size).
+ */
+comp_status_t comp_gemm_f32x16_variant(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N,
+                                       int64_t K, int variant, comp_stream_t stream);
+
+/*
+ * comp_device_status — waits for `stream`, then reports and clears the fault
+ * word that kernels of this library set when a bounded wait inside them gives
+ * up (they then skip the rest of their work and exit cleanly, leaving the
+ * context usable).  Returns COMP_OK, COMP_ERR_TIMEOUT, or COMP_ERR_CUDA if the
+ * stream itself reported an error.  If `where` is not NULL it receives the
+ * fault word (0 when clear; otherwise a code naming the wait that gave up).
+ */
+comp_status_t comp_device_status(comp_stream_t stream, uint32_t* where);
+
+/* Human-readable name of a status code (a static string). */
+const char* comp_status_string(comp_status_t status);
+
+/* The library's version as major*10000 + minor*100 + patch. */
+int comp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COMPFP32_H */

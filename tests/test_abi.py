@@ -1,0 +1,100 @@
+"""The C ABI library on the host: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments before touching any device (these
+calls never launch a kernel, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "compfp32.h")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    from compensated_fp32_projection_gb300 import _native, build
+
+    build.build()
+    return _native.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(comp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = _declared()
+    for n in ("comp_split_f32", "comp_merge_f32", "comp_gemm_f32x16", "comp_gemm_f32_simt", "comp_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from compensated_fp32_projection_gb300 import _native
+
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in _native.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings_and_version(lib):
+    for code in range(6):
+        s = lib.comp_status_string(code).decode()
+        assert s.startswith("COMP_")
+    assert lib.comp_version() >= 100
+
+
+P = ctypes.c_void_p
+
+
+def test_split_argument_errors(lib):
+    # negative size, NULL pointers, overlapping outputs: rejected before any device work
+    assert lib.comp_split_f32(P(4096), P(1 << 20), P(1 << 21), -1, None) == 1
+    assert lib.comp_split_f32(None, P(1 << 20), P(1 << 21), 8, None) == 1
+    assert lib.comp_split_f32(P(4096), None, P(1 << 21), 8, None) == 1
+    assert lib.comp_split_f32(P(4096), P(1 << 20), P(1 << 20) , 8, None) == 1  # hi == lo
+    assert lib.comp_split_f32(P(4096), P(4096 + 8), P(1 << 21), 8, None) == 1  # hi inside x
+    assert lib.comp_split_f32(P(4096), P(1 << 20), P((1 << 20) + 14), 8, None) == 1  # lo overlaps hi
+    assert lib.comp_split_f32(None, None, None, 0, None) == 0  # empty is a no-op
+
+
+def test_merge_argument_errors(lib):
+    assert lib.comp_merge_f32(P(4096), P(1 << 20), P(1 << 21), -5, None) == 1
+    assert lib.comp_merge_f32(None, P(1 << 20), P(1 << 21), 4, None) == 1
+    assert lib.comp_merge_f32(P(4096), P(1 << 20), P(4096 + 4), 4, None) == 1  # partial overlap with acc_hi
+    assert lib.comp_merge_f32(P(4096), P(1 << 20), P((1 << 20) - 4), 4, None) == 1  # partial overlap with acc_lo
+    assert lib.comp_merge_f32(None, None, None, 0, None) == 0
+
+
+def test_gemm_argument_errors(lib):
+    for fn in (lib.comp_gemm_f32x16, lib.comp_gemm_f32_simt):
+        assert fn(P(4096), P(1 << 20), P(1 << 24), -1, 4, 4, None) == 1
+        assert fn(P(4096), P(1 << 20), P(1 << 24), 4, -1, 4, None) == 1
+        assert fn(P(4096), P(1 << 20), P(1 << 24), 4, 4, -1, None) == 1
+        assert fn(None, P(1 << 20), P(1 << 24), 4, 4, 4, None) == 1
+        assert fn(P(4096), P(1 << 20), None, 4, 4, 4, None) == 1
+        assert fn(P(4096), P(1 << 20), P(4096 + 16), 4, 4, 4, None) == 1  # y overlaps x
+        assert fn(P(4096), P(1 << 20), P((1 << 20) + 4), 4, 4, 4, None) == 1  # y overlaps W
+        assert fn(P(4096), P(1 << 20), P(1 << 24), 1 << 40, 1 << 40, 4, None) == 1  # M*N overflows
+        assert fn(P(4096), P(1 << 20), P(1 << 24), 1 << 31, 4, 4, None) == 1  # M beyond int32
+        assert fn(None, None, None, 0, 5, 7, None) == 0  # empty output: no-op
+    assert lib.comp_gemm_f32x16_variant(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, 7, None) == 1
+
+
+def test_no_device_is_an_error_not_a_fallback(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid arguments on a host without a usable sm_103 device: an error, never a CPU path
+    assert lib.comp_split_f32(P(4096), P(1 << 20), P(1 << 21), 8, None) == 2
+    assert lib.comp_gemm_f32x16(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, None) == 2
+
+
+def test_package_import_does_not_need_the_library():
+    import compensated_fp32_projection_gb300 as pkg
+
+    assert callable(pkg.comp_gemm_f32x16)

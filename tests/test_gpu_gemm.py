@@ -1,0 +1,226 @@
+"""GPU parity of the fused compensated projection and the true-FP32 SIMT GEMM.
+
+Gate (the method's acceptance for the projection, laya.cpp docs/vulkan.md,
+compensated-FP32 paragraph, with the stated tolerance): every element of the
+fused kernel's y satisfies |y - y_oracle| <= 4e-6 * sum_k |x_k||w_k| + 1e-30,
+where y_oracle is the oracle's FP64 evaluation of the same formula, and the
+max-normalised error against the true product is at least 100x smaller than
+that of a single FP16 cast of x.
+
+The SIMT GEMM is the true-FP32 reference (paragraph on the true FP32 matrix
+kernels): within the recursive-summation bound gamma_K * sum|x||w|,
+gamma_K = K u / (1 - K u), u = 2^-24, of the exact product.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+TOL = 4e-6
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import compensated_fp32_projection_gb300 as p
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return p
+
+
+def w_bits(W):
+    return W.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def check_comp(y, x, W, orc, rows=None, cols=None):
+    """Elementwise gate against the oracle; returns (gpu error, cast error) max-normalised vs the true product."""
+    xn, wn = x.cpu().numpy(), w_bits(W)
+    yg = y.detach().cpu().numpy()
+    if rows is not None:
+        yg = yg[rows, cols]
+    y_or = orc.gemm_comp(xn, wn, rows, cols).astype(np.float64)
+    den = orc.gemm_den(xn, wn, rows, cols)
+    err = np.abs(yg.astype(np.float64) - y_or)
+    bound = TOL * den + 1e-30
+    bad = np.argwhere(~(err <= bound))
+    assert bad.size == 0, (
+        f"{bad.shape[0]} elements over tolerance; first {bad[:3].tolist()}, "
+        f"worst ratio {float(np.nanmax(err / bound))}"
+    )
+    y_true = orc.gemm_true(xn, wn, rows, cols).astype(np.float64)
+    y_cast = orc.gemm_cast(xn, wn, rows, cols).astype(np.float64)
+    e_gpu = float(np.max(np.abs(yg - y_true) / (den + 1e-30)))
+    e_cast = float(np.max(np.abs(y_cast - y_true) / (den + 1e-30)))
+    return e_gpu, e_cast
+
+
+def gemm(pkg, x, W, variant):
+    if variant is None:
+        return pkg.comp_gemm_f32x16(x, W)
+    return pkg.comp_gemm_f32x16_variant(x, W, variant)
+
+
+@pytest.mark.parametrize("name", ["tiny", "encoder", "nonaligned"])
+def test_projection_shapes_full(pkg, orc, name):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs(name)
+    y = pkg.comp_gemm_f32x16(x.cuda(), W.cuda())
+    e_gpu, e_cast = check_comp(y, x, W, orc)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+
+
+@pytest.mark.parametrize("name", ["square", "skinny"])
+def test_projection_shapes_sampled(pkg, orc, name):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs(name)
+    y = pkg.comp_gemm_f32x16(x.cuda(), W.cuda())
+    M, N = x.shape[0], W.shape[0]
+    rng = np.random.default_rng(5)
+    # random samples plus the corners and edges of the output
+    r = np.concatenate([rng.integers(0, M, 3000), [0, 0, M - 1, M - 1], np.full(16, M - 1), np.arange(min(M, 16))])
+    c = np.concatenate([rng.integers(0, N, 3000), [0, N - 1, 0, N - 1], np.arange(N - 16, N), np.full(min(M, 16), N - 1)])
+    order = np.argsort(r, kind="stable")
+    e_gpu, e_cast = check_comp(y, x, W, orc, r[order], c[order])
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+    assert torch.isfinite(y).all()
+
+
+SHAPES = [
+    (1, 1, 1),
+    (1, 1, 8),
+    (3, 5, 7),
+    (8, 384, 256),
+    (128, 256, 64),
+    (130, 300, 72),
+    (257, 513, 200),
+    (129, 257, 1027),
+    (200, 1000, 520),
+    (17, 260, 4096),
+    (384, 768, 24),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("variant", [None, 1, 2])
+def test_tiles_and_ragged_tails(pkg, orc, shape, variant):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    if variant == 1 and K % 8 != 0:
+        pytest.skip("TMA path needs K % 8 == 0")
+    x, W = workloads.random_case(M, N, K, seed=M * 1_000_003 + N * 101 + K, scale=3.0)
+    y = gemm(pkg, x.cuda(), W.cuda(), variant)
+    check_comp(y, x, W, orc)
+
+
+def test_tma_and_plain_paths_agree_bitwise(pkg):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.random_case(300, 520, 264, seed=9)
+    x, W = x.cuda(), W.cuda()
+    y1 = pkg.comp_gemm_f32x16_variant(x, W, 1)
+    y2 = pkg.comp_gemm_f32x16_variant(x, W, 2)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+
+
+def test_deterministic(pkg):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs("encoder")
+    x, W = x.cuda(), W.cuda()
+    y1 = pkg.comp_gemm_f32x16(x, W)
+    y2 = pkg.comp_gemm_f32x16(x, W)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+
+
+def test_exact_fp16_inputs_match_fp16_product(pkg, orc):
+    # x exact in FP16: lo = 0, so y is a plain FP16 product with FP32 accumulation
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.random_case(256, 512, 512, seed=3)
+    x = x.half().float()
+    y = pkg.comp_gemm_f32x16(x.cuda(), W.cuda())
+    check_comp(y, x, W, orc)
+
+
+def test_one_hot_rows_select_weights(pkg):
+    # x = I (K x K): y[i, j] = W[j, i] exactly
+    K, N = 192, 320
+    W = (torch.randn(N, K) * 0.02).half()
+    x = torch.eye(K, dtype=torch.float32)
+    y = pkg.comp_gemm_f32x16(x.cuda(), W.cuda()).cpu()
+    assert torch.equal(y, W.float().t())
+
+
+def test_identity_weights_reconstruct_x(pkg):
+    K = 256
+    x = torch.randn(200, K) * 50
+    W = torch.eye(K, dtype=torch.float16)
+    y = pkg.comp_gemm_f32x16(x.cuda(), W.cuda()).cpu().double()
+    xd = x.double()
+    assert torch.all((y - xd).abs() <= 2.0**-22 * xd.abs() + 2.0**-35)
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop(pkg):
+    x = torch.empty(4, 0, device="cuda")
+    W = torch.empty(6, 0, dtype=torch.float16, device="cuda")
+    y = torch.full((4, 6), 7.0, device="cuda")
+    pkg.comp_gemm_f32x16(x, W, y)
+    assert torch.equal(y.cpu(), torch.zeros(4, 6))
+    x0 = torch.empty(0, 16, device="cuda")
+    y0 = pkg.comp_gemm_f32x16(x0, torch.ones(5, 16, dtype=torch.float16, device="cuda"))
+    assert y0.shape == (0, 5)
+
+
+def test_output_guard_bands(pkg, orc):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = 130, 300, 72
+    x, W = workloads.random_case(M, N, K, seed=77)
+    pad = 4096
+    buf = torch.full((M * N + 2 * pad,), float("nan"), device="cuda")
+    y = buf[pad:pad + M * N].view(M, N)
+    pkg.comp_gemm_f32x16(x.cuda(), W.cuda(), y)
+    check_comp(y, x, W, orc)
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + M * N:]).all()
+
+
+def test_large_and_tiny_magnitudes(pkg, orc):
+    # the non-aligned shape's mix, at a multi-tile size: |x| up to 6e4 next to 1e-6
+    g = torch.Generator().manual_seed(11)
+    M, N, K = 300, 520, 1000
+    big = torch.rand((M, K), generator=g) * 1.2e5 - 6e4
+    small = torch.randn((M, K), generator=g) * 1e-6
+    x = torch.where(torch.rand((M, K), generator=g) < 0.5, small, big)
+    W = (torch.randn((N, K), generator=g) * 0.02).half()
+    for variant in (1, 2):
+        y = pkg.comp_gemm_f32x16_variant(x.cuda(), W.cuda(), variant)
+        e_gpu, e_cast = check_comp(y, x, W, orc)
+        assert e_cast >= 100 * e_gpu
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (3, 5, 7), (130, 300, 72), (129, 257, 1027), (512, 1024, 1024)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_simt_true_fp32(pkg, orc, shape):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=K + 5, scale=2.0)
+    y = pkg.comp_gemm_f32_simt(x.cuda(), W.cuda()).cpu().numpy().astype(np.float64)
+    xn, wn = x.numpy(), w_bits(W)
+    y_true = xn.astype(np.float64) @ wn.view(np.float16).astype(np.float64).T
+    den = orc.gemm_den(xn, wn)
+    u = 2.0**-24
+    gamma = K * u / (1 - K * u)
+    assert np.all(np.abs(y - y_true) <= gamma * den + 2.0**-149)
+
+
+def test_device_status_clean_after_gemms(pkg):
+    st, where = pkg.device_status()
+    assert st == 0 and where == 0
