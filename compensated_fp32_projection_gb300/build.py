@@ -74,6 +74,25 @@ def _compile(src: str) -> tuple[str, str]:
     return obj, p.stderr
 
 
+# Kernels that move registers between warpgroups with setmaxnreg assume this
+# launch register count; a different count could make setmaxnreg.inc wait
+# forever, so the build refuses it.
+SETMAXNREG_KERNELS = {"comp_gemm_kernel": 96}
+
+
+def _check_register_budget(ptxas_log: str) -> None:
+    current = None
+    for line in ptxas_log.splitlines():
+        if "Compiling entry function" in line:
+            current = next((k for k in SETMAXNREG_KERNELS if k in line), None)
+        elif current and "Used" in line and "registers" in line:
+            used = int(line.split("Used")[1].split("registers")[0])
+            if used != SETMAXNREG_KERNELS[current]:
+                raise RuntimeError(f"{current}: ptxas reports {used} registers, the register split assumes "
+                                   f"{SETMAXNREG_KERNELS[current]}")
+            current = None
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link the library if any source changed; returns its path."""
     if not force and up_to_date():
@@ -85,6 +104,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with open(os.path.join(BUILD, "ptxas.txt"), "w") as f:
         for (obj, log), src in zip(results, srcs):
             f.write(f"== {os.path.basename(src)}\n{log}\n")
+    _check_register_budget("\n".join(log for _, log in results))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     p = subprocess.run(cmd, capture_output=True, text=True)

@@ -1,31 +1,42 @@
-// The fused compensated-FP32 projection on the fifth-generation tensor cores
-// (laya.cpp docs/vulkan.md: the compensated-FP32 paragraph — two FP16
-// components per input, both products with FP32 accumulators, combined in FP32
-// — and "The fused split/merge build" paragraph — split and merge fused into
-// the projection).
+// The fused compensated-FP32 projection on the fifth-generation tensor cores.
 //
-// One CTA computes a 128 x 256 tile of y = acc_hi + acc_lo * 2^-10:
-//   warp 0      TMA producer: per K block of 64, one 256x64 FP16 box of W and
-//               two 128x32 FP32 boxes of x into a pipeline stage (128-byte
-//               swizzle), completion counted on the stage's `full` barrier;
-//   warp 1      allocates 512 TMEM columns (two 128x256 FP32 accumulators) and,
-//               from one thread, issues per K block 4 x 2 tcgen05.mma
-//               (M=128, N=256, K=16): D_hi += hi*W^T, D_lo += lo*W^T, both
-//               reading the same W descriptor; a commit frees the stage;
-//   warps 2..5  split: each thread owns one row of the stage's x tile, reads
-//               its 64 FP32 values, and writes hi = fp16_rne(x) and
-//               lo = fp16_rne((x - hi) * 1024) in place, in the K-major
-//               128-byte-swizzled layout the MMA reads (hi over the first 16
-//               KB of the x area, lo over the second); then they run the
-//               epilogue: tcgen05.ld of both accumulators, the merge
-//               y = D_hi + D_lo * 2^-10 (two rounded FP32 operations), store.
-// The plain-load variant (any alignment / K) has no producer warp: the split
-// warps stage x and W with coalesced, bounds-checked loads into the same
-// layout and then split as above.
+// Method (laya.cpp, docs/vulkan.md):
+//   - compensated-FP32 paragraph: each FP32 input is split into two FP16
+//     components, both products with the exact FP16 weights accumulate in FP32,
+//     and the two are combined in FP32;
+//   - "The fused split/merge build" paragraph: split and merge fused into the
+//     projection;
+//   - AMD paragraph: accumulating tile results with separate FP32 additions,
+//     rather than one long chain of cooperative-matrix multiply-adds, removes the
+//     accumulation drift of long dot products.
 //
-// Every mbarrier wait is bounded: past about a second the waiting thread
-// records a fault code, raises the CTA's abort flag, and all roles skip to the
-// end, drain what they issued (also bounded) and free TMEM.
+// A persistent CTA computes 128 x BN tiles of y.  Per tile and K block of 64:
+//   1. TMA brings the 128 x 64 FP32 block of x (two 128x32 boxes, 128-byte
+//      swizzle) into a 4-deep shared-memory ring, and the BN x 64 FP16 box of W
+//      into another 4-deep ring;
+//   2. eight split warps (two per 32-row quarter, one half of the K block
+//      each), one thread per row, read their part of the row of x, form
+//      hi = fp16_rne(x) and lo = fp16_rne((x - hi) * 1024), and store both
+//      into tensor memory (tcgen05.st), where the MMA reads its A operand;
+//   3. one thread issues 8 tcgen05.mma (M=128, N=BN, K=16, A from tensor
+//      memory, B = W from shared memory) into a fresh accumulator D: four for
+//      lo*W^T (the first overwrites D), then four for hi*W^T, the first of
+//      which scales the accumulator by 2^-10 on input, so that
+//      D = hi*W^T + 2^-10 * (lo*W^T) for the block; both products read the
+//      same W descriptor.  D is double-buffered, the A operand triple-buffered;
+//   4. eight promotion warps read D (tcgen05.ld, all of a warp's columns in
+//      one round trip) and add it to an FP32 register accumulator R with
+//      round-to-nearest-even adds, one FP32 add per K block outside the tensor
+//      core; after the tile's last block R is y.
+// Tensor memory: D buffers at columns [0, 2*BN), A stages at [320, 512)
+// (64 columns each: hi in the first 32, lo in the next 32).
+//
+// The plain-load variant (any alignment, any K) stages W and x with ordinary
+// bounds-checked loads done by the split warps instead of TMA.
+//
+// Every mbarrier wait is bounded: after about a second the waiting thread
+// records a fault code, raises the CTA's abort flag, and every role skips to
+// the end, drains what it issued (bounded) and frees tensor memory.
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -37,35 +48,69 @@ namespace compfp32 {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int kStages = 3;
-constexpr int kSplitWarps = 4;
-constexpr int kThreads = 64 + 32 * kSplitWarps;
-constexpr uint32_t kWBytes = BN * BK * 2;             // 32 KB: W box, FP16
-constexpr uint32_t kABytes = BM * BK * 4;             // 32 KB: x as FP32, later hi | lo as FP16
-constexpr uint32_t kHalfA = kABytes / 2;              // 16 KB: one 128x32 FP32 box / one 128x64 FP16 plane
-constexpr uint32_t kStageBytes = kWBytes + kABytes;   // 64 KB
+constexpr int kPromoters = 8;  // warpgroups 1-2: promote the accumulator, store y
+constexpr int kSplitters = 8;  // warpgroups 3-4: split x into hi/lo in tensor memory
+constexpr int kThreads = 128 + 32 * (kPromoters + kSplitters);  // warpgroup 0: W and x producers, MMA issuer
+// Register split between warpgroups (setmaxnreg).  The launch gives every
+// thread 96 registers (640 threads, one CTA per SM), a pool of 61440; the
+// control warpgroup drops to 24, the promotion warpgroups rise to 168 and the
+// split warpgroups drop to 56: 128*24 + 256*168 + 256*56 = 60416 <= 61440.
+// The build checks the 96.
+constexpr int kLaunchRegs = 96;
+constexpr int kCtrlRegs = 24;
+constexpr int kPromoRegs = 168;
+constexpr int kSplitRegs = 56;
+static_assert(128 * kCtrlRegs + 32 * kPromoters * kPromoRegs + 32 * kSplitters * kSplitRegs <=
+                  kThreads * kLaunchRegs,
+              "register split");
+constexpr int kWStages = 4;
+constexpr int kXStages = 4;
+constexpr uint32_t kXBytes = BM * BK * 4;  // 32 KB: two 128x32 FP32 boxes
+constexpr uint32_t kXBox = kXBytes / 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + 256 /* barriers */;
+constexpr int kAStageCols = 64;            // one A stage: hi (32 columns) + lo (32 columns)
 constexpr long long kWaitLimit = 1ll << 31;  // cycles (about a second)
 
+template <int BN>
+struct Cfg {
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 160, "BN");
+    static constexpr uint32_t kWBytes = BN * BK * 2;
+    static constexpr size_t kSmem = 1024 + kWStages * kWBytes + kXStages * kXBytes + 512;
+    static_assert(kSmem <= 232448, "shared memory");
+    static constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
+    static constexpr int kHalf = BN / 2;  // accumulator columns per promotion warp
+    // Tensor memory: two accumulator buffers, then as many A stages as fit.
+    static constexpr uint32_t kACol = 2 * BN;
+    static constexpr int kAStages = static_cast<int>((kTmemCols - kACol) / kAStageCols) > 4
+                                        ? 4
+                                        : static_cast<int>((kTmemCols - kACol) / kAStageCols);
+    static_assert(kAStages >= 2, "A stages");
+};
+
 // Fault codes (the wait that gave up).
-constexpr uint32_t kFaultProducerEmpty = 0x101;
-constexpr uint32_t kFaultSplitFull = 0x201;
-constexpr uint32_t kFaultSplitEmpty = 0x202;
-constexpr uint32_t kFaultMmaReady = 0x301;
-constexpr uint32_t kFaultEpilogue = 0x401;
+constexpr uint32_t kFaultWProducer = 0x101;
+constexpr uint32_t kFaultXProducer = 0x102;
+constexpr uint32_t kFaultMmaW = 0x301;
+constexpr uint32_t kFaultMmaA = 0x302;
+constexpr uint32_t kFaultMmaD = 0x303;
+constexpr uint32_t kFaultSplitX = 0x201;
+constexpr uint32_t kFaultSplitA = 0x202;
+constexpr uint32_t kFaultSplitW = 0x203;
+constexpr uint32_t kFaultPromote = 0x401;
 
 __device__ uint32_t g_fault_word;
 
 struct Barriers {
-    uint64_t full[kStages];   // TMA bytes landed (count 1 + tx)
-    uint64_t ready[kStages];  // hi/lo written (count kSplitWarps)
-    uint64_t empty[kStages];  // MMAs of the stage completed (tcgen05.commit)
-    uint64_t acc;             // all MMAs of the tile completed
-    uint64_t drain;           // MMA drain on abort
+    uint64_t wfull[kWStages];   // W box landed (TMA bytes) / staged (plain path: split warps)
+    uint64_t wempty[kWStages];  // MMAs reading the W stage completed
+    uint64_t xfull[kXStages];   // x block landed (TMA bytes)
+    uint64_t xempty[kXStages];  // split warps have read the x stage
+    uint64_t aready[4];         // hi/lo of a K block are in tensor memory
+    uint64_t aempty[4];         // MMAs reading the A stage completed
+    uint64_t dfull[2];          // accumulator buffer holds a finished K block
+    uint64_t dfree[2];          // promotion warps have read the accumulator buffer
+    uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -76,7 +121,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Bar
         return true;
     const long long start = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_sleep(bar, parity, 20000))
             return true;
         if (*reinterpret_cast<volatile int*>(&b->abort))
             return false;
@@ -88,25 +133,35 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Bar
     }
 }
 
-__device__ __forceinline__ bool aborted(Barriers* b)
+// Warp-wide bounded wait: lane 0 polls, the verdict is broadcast, and on
+// success every lane performs one (immediately successful) try_wait so that it
+// observes the phase completion itself.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Barriers* b, uint32_t code)
 {
-    return *reinterpret_cast<volatile int*>(&b->abort) != 0;
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0)
+        ok = wait_bounded(bar, parity, b, code);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (ok)
+        (void)mbar_try_wait(bar, parity);
+    return ok;
 }
 
-// Barrier over the kSplitWarps split warps (named barrier 1) that also returns
-// the AND of `v` over all of them.
-__device__ __forceinline__ bool split_warps_all(bool v)
+// Bounded wait for the copies or MMAs a role already issued before the CTA
+// exits after an abort; no fault code (the first failure has one).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
 {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.and.pred p, 1, %2, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "n"(32 * kSplitWarps)
-        : "memory");
-    return r != 0;
+    const long long start = clock64();
+    while (!mbar_try_wait(bar, parity) && clock64() - start < kWaitLimit) {
+    }
+}
+
+// 16-byte load from shared memory at a 32-bit shared-window address.
+__device__ __forceinline__ float4 lds128(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 h)
@@ -114,113 +169,196 @@ __device__ __forceinline__ uint32_t pack_h2(__half2 h)
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Byte offset of the 16-byte chunk `chunk` of row `row` in a tile of 128-byte
-// rows with the 128-byte swizzle (the tile base is 1024-byte aligned).
+// Byte offset of 16-byte chunk `chunk` of row `row` in a tile of 128-byte rows
+// with the 128-byte swizzle (tile base 1024-byte aligned).
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk)
 {
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
-// In-place split of one row of the stage's A area: reads the 64 FP32 values of
-// row r (two 128x32 boxes), writes 64 hi values to plane 0 and 64 lo values to
-// plane 1, each plane a 128x64 FP16 tile.  A thread only touches the bytes of
-// its own row, so no other synchronisation is needed.
-__device__ __forceinline__ void split_row_inplace(uint8_t* A, uint32_t r)
+__device__ __forceinline__ uint64_t f2_bits(float a, float b)
 {
-    float v[64];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {  // 16 chunks of 4 FP32: chunk c is k = 4c .. 4c+3
-        const float4 q = *reinterpret_cast<const float4*>(A + (c >> 3) * kHalfA + sw128(r, c & 7));
-        v[4 * c + 0] = q.x;
-        v[4 * c + 1] = q.y;
-        v[4 * c + 2] = q.z;
-        v[4 * c + 3] = q.w;
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {  // 8 chunks of 8 FP16: chunk c is k = 8c .. 8c+7
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float a = v[8 * c + 2 * p], b = v[8 * c + 2 * p + 1];
-            const __half2 hh = __floats2half2_rn(a, b);
-            const float2 hf = __half22float2(hh);
-            const float ra = __fmul_rn(__fsub_rn(a, hf.x), 1024.0f);
-            const float rb = __fmul_rn(__fsub_rn(b, hf.y), 1024.0f);
-            h[p] = pack_h2(hh);
-            l[p] = pack_h2(__floats2half2_rn(ra, rb));
-        }
-        *reinterpret_cast<uint4*>(A + sw128(r, c)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(A + kHalfA + sw128(r, c)) = make_uint4(l[0], l[1], l[2], l[3]);
-    }
+    return static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
 }
 
-// Plain-load staging of one K block by the split warps (128 threads):
-// x rows m0..m0+127, k0..k0+63 as FP32 into the two 128x32 swizzled boxes,
-// W rows n0..n0+255 as FP16 into the 256x64 swizzled tile; zero outside.
-__device__ __forceinline__ void stage_plain(uint8_t* Wt, uint8_t* A, const float* __restrict__ x,
-                                            const uint16_t* __restrict__ W, int64_t M, int64_t N, int64_t K,
-                                            int64_t m0, int64_t n0, int64_t k0, int sw, int lane)
+__device__ __forceinline__ float lo_f(uint64_t v)
 {
-    // x: warp sw handles rows sw, sw+4, ...; lane covers k0+lane and k0+32+lane
-#pragma unroll 4
-    for (int r = sw; r < BM; r += kSplitWarps) {
-        const int64_t m = m0 + r;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t k = k0 + h * 32 + lane;
-            const float v = (m < M && k < K) ? x[m * K + k] : 0.0f;
-            *reinterpret_cast<float*>(A + h * kHalfA + sw128(r, lane >> 2) + (lane & 3) * 4) = v;
-        }
-    }
-    // W: lane covers the FP16 pair k0+2*lane, k0+2*lane+1
-#pragma unroll 4
-    for (int r = sw; r < BN; r += kSplitWarps) {
-        const int64_t n = n0 + r;
-        const int64_t k = k0 + 2 * lane;
-        uint32_t lo16 = 0, hi16 = 0;
-        if (n < N) {
-            const uint16_t* row = W + n * K;
-            if (k < K)
-                lo16 = row[k];
-            if (k + 1 < K)
-                hi16 = row[k + 1];
-        }
-        *reinterpret_cast<uint32_t*>(Wt + sw128(r, lane >> 2) + (lane & 3) * 4) = lo16 | (hi16 << 16);
-    }
+    return __uint_as_float(static_cast<uint32_t>(v));
 }
 
-template <bool kTma>
+__device__ __forceinline__ float hi_f(uint64_t v)
+{
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+
+// Split two consecutive values (a first): packed FP16 pairs hi and lo.
+// The residual (a - hi) * 1024 is computed on both lanes at once, each
+// operation rounded to nearest even and never fused (exact here: the
+// difference and the scaling by a power of two are representable).
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo)
+{
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 hf = __half22float2(h);
+    uint64_t d, r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a, b)), "l"(f2_bits(hf.x, hf.y)));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(d), "l"(f2_bits(1024.0f, 1024.0f)));
+    hi = pack_h2(h);
+    lo = pack_h2(__floats2half2_rn(lo_f(r), hi_f(r)));
+}
+
+// Two element-wise RNE FP32 additions: r0 += v0, r1 += v1.
+__device__ __forceinline__ void add2(float& r0, float& r1, uint32_t v0, uint32_t v1)
+{
+    uint64_t s;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(s)
+        : "l"(f2_bits(r0, r1)), "l"(f2_bits(__uint_as_float(v0), __uint_as_float(v1))));
+    r0 = lo_f(s);
+    r1 = hi_f(s);
+}
+
+// Warp-wide: 32 TMEM lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D (+)= A * B^T with A (128 x 16 FP16) in tensor memory and B in shared memory.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D = A * B^T + D * 2^-10 (accumulator input scaled by 2^-10), A in tensor memory.
+__device__ __forceinline__ void umma_f16_ta_scale10(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, 1, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p, 10;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc)
+        : "memory");
+}
+
+struct Problem {
+    const float* x;
+    const uint16_t* W;
+    float* y;
+    int M, N, K;
+    int tiles_m, tiles_n, nk;
+    int vec_y;
+};
+
+// Tile t covers rows (t / tiles_n) * 128 .. and columns (t % tiles_n) * BN ..;
+// N runs fastest so that CTAs working at the same time share rows of x.
+__device__ __forceinline__ int tile_m(int t, const Problem& P)
+{
+    return t / P.tiles_n;
+}
+__device__ __forceinline__ int tile_n(int t, const Problem& P)
+{
+    return t % P.tiles_n;
+}
+
+// Walks this CTA's K blocks in order (tiles blockIdx.x, + gridDim.x, ...; K
+// blocks 0 .. nk-1 of each), dividing only when the tile changes.
+template <int BN>
+struct Cursor {
+    int t, kb, m0, n0;  // tile, K block, first row, first column
+    __device__ __forceinline__ void start(const Problem& P)
+    {
+        t = static_cast<int>(blockIdx.x);
+        kb = 0;
+        m0 = tile_m(t, P) * BM;
+        n0 = tile_n(t, P) * BN;
+    }
+    __device__ __forceinline__ void next(const Problem& P)
+    {
+        if (++kb == P.nk) {
+            kb = 0;
+            t += static_cast<int>(gridDim.x);
+            m0 = tile_m(t, P) * BM;
+            n0 = tile_n(t, P) * BN;
+        }
+    }
+};
+
+template <int BN, bool kVec>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                   const float* __restrict__ x, const uint16_t* __restrict__ W, float* __restrict__ y, int64_t M,
-                   int64_t N, int64_t K, int vec_y)
+    comp_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                     const Problem P)
 {
+    using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Barriers* bars = reinterpret_cast<Barriers*>(smem + kStages * kStageBytes);
-    auto stage_w = [&](int s) { return smem + s * kStageBytes; };
-    auto stage_a = [&](int s) { return smem + s * kStageBytes + kWBytes; };
+    uint8_t* wring = smem;                          // kWStages x BN x 128 B
+    uint8_t* xring = smem + kWStages * C::kWBytes;  // kXStages x 32 KB
+    Barriers* bars = reinterpret_cast<Barriers*>(xring + kXStages * kXBytes);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * BN;
-    const int num_kb = static_cast<int>((K + BK - 1) / BK);
+    const int num_tiles = P.tiles_m * P.tiles_n;
+    const int my_tiles =
+        static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const int total = my_tiles * P.nk;  // K blocks this CTA processes
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->ready[s], kSplitWarps);
-            mbar_init(&bars->empty[s], 1);
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&bars->wfull[s], kVec ? 1 : kSplitters);
+            mbar_init(&bars->wempty[s], 1);
         }
-        mbar_init(&bars->acc, 1);
+        for (int s = 0; s < kXStages; ++s) {
+            mbar_init(&bars->xfull[s], 1);
+            mbar_init(&bars->xempty[s], kSplitters);
+        }
+        for (int a = 0; a < C::kAStages; ++a) {
+            mbar_init(&bars->aready[a], kSplitters);
+            mbar_init(&bars->aempty[a], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->dfull[b], 1);
+            mbar_init(&bars->dfree[b], kPromoters);
+        }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
-        if (kTma) {
-            tma_prefetch_desc(&tmap_x);
+        if (kVec) {
             tma_prefetch_desc(&tmap_w);
+            tma_prefetch_desc(&tmap_x);
         }
     }
     if (warp == 1) {
@@ -232,127 +370,221 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (kTma && lane == 0) {
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+        if (kVec && (warp == 0 || warp == 2) && lane == 0) {
+            // ---------------- TMA producers: W (warp 0) and x (warp 2) ----------------
+            const bool is_w = warp == 0;
+            const int depth = is_w ? kWStages : kXStages;
+            uint64_t* full = is_w ? bars->wfull : bars->xfull;
+            uint64_t* empty = is_w ? bars->wempty : bars->xempty;
             int issued = 0;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t round = static_cast<uint32_t>(kb / kStages);
-                if (kb >= kStages && !wait_bounded(&bars->empty[s], (round - 1) & 1, bars, kFaultProducerEmpty))
+            Cursor<BN> cur;
+            cur.start(P);
+            for (int g = 0; g < total; ++g, cur.next(P)) {
+                const int s = g % depth;
+                if (g >= depth &&
+                    !wait_bounded(&empty[s], ((g / depth) - 1) & 1, bars, is_w ? kFaultWProducer : kFaultXProducer))
                     break;
-                mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
-                tma_load_2d(stage_w(s), &tmap_w, &bars->full[s], kb * BK, static_cast<int32_t>(n0));
-                tma_load_2d(stage_a(s), &tmap_x, &bars->full[s], kb * BK, static_cast<int32_t>(m0));
-                tma_load_2d(stage_a(s) + kHalfA, &tmap_x, &bars->full[s], kb * BK + 32, static_cast<int32_t>(m0));
-                issued = kb + 1;
-            }
-            if (aborted(bars)) {
-                // let the copies still in flight land before the CTA exits
-                for (int kb = issued - kStages < 0 ? 0 : issued - kStages; kb < issued; ++kb) {
-                    const int s = kb % kStages;
-                    const uint32_t round = static_cast<uint32_t>(kb / kStages);
-                    const long long start = clock64();
-                    while (!mbar_try_wait(&bars->full[s], round & 1) && clock64() - start < kWaitLimit) {
-                    }
+                const int k0 = cur.kb * BK;
+                if (is_w) {
+                    mbar_arrive_expect_tx(&full[s], C::kWBytes);
+                    tma_load_2d(wring + s * C::kWBytes, &tmap_w, &full[s], k0, cur.n0);
+                } else {
+                    mbar_arrive_expect_tx(&full[s], kXBytes);
+                    uint8_t* dst = xring + s * kXBytes;
+                    tma_load_2d(dst, &tmap_x, &full[s], k0, cur.m0);
+                    tma_load_2d(dst + kXBox, &tmap_x, &full[s], k0 + 32, cur.m0);
                 }
+                issued = g + 1;
             }
-        }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            int kb = 0;
-            for (; kb < num_kb; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t round = static_cast<uint32_t>(kb / kStages);
-                if (!wait_bounded(&bars->ready[s], round & 1, bars, kFaultMmaReady))
+            if (*reinterpret_cast<volatile int*>(&bars->abort))
+                for (int g = issued - depth < 0 ? 0 : issued - depth; g < issued; ++g)
+                    drain_wait(&full[g % depth], (g / depth) & 1);
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- MMA issuer ----------------
+            // B descriptors: stage s, K step j = desc of stage 0 + (s * stage bytes + 32 j) / 16 in the
+            // start-address field (no carry: shared addresses stay below 2^18).
+            const uint64_t wdesc0 = sw128_kmajor_desc(smem_u32(wring));
+            bool ok = true;
+            for (int g = 0; g < total && ok; ++g) {
+                const int sw = g % kWStages;
+                const int sa = g % C::kAStages;  // A stage
+                const int b = g & 1;          // accumulator buffer
+                ok = wait_bounded(&bars->wfull[sw], (g / kWStages) & 1, bars, kFaultMmaW) &&
+                     wait_bounded(&bars->aready[sa], (g / C::kAStages) & 1, bars, kFaultMmaA) &&
+                     (g < 2 || wait_bounded(&bars->dfree[b], ((g >> 1) - 1) & 1, bars, kFaultMmaD));
+                if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t a_base = smem_u32(stage_a(s));
-                const uint32_t w_base = smem_u32(stage_w(s));
+                const uint32_t d = tmem + b * BN;
+                const uint32_t a_hi = tmem + C::kACol + sa * 64;
+                const uint32_t a_lo = a_hi + 32;
+                const uint64_t bd = wdesc0 + static_cast<uint64_t>(sw * (C::kWBytes >> 4));
 #pragma unroll
-                for (int j = 0; j < BK / 16; ++j) {
-                    const uint64_t bdesc = sw128_kmajor_desc(w_base + 32 * j);
-                    const uint64_t hdesc = sw128_kmajor_desc(a_base + 32 * j);
-                    const uint64_t ldesc = sw128_kmajor_desc(a_base + kHalfA + 32 * j);
-                    const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
-                    umma_f16(tmem, hdesc, bdesc, kIdesc, accum);
-                    umma_f16(tmem + BN, ldesc, bdesc, kIdesc, accum);
-                }
-                umma_commit(&bars->empty[s]);
+                for (int j = 0; j < BK / 16; ++j)  // lo * W^T, the first overwrites D
+                    umma_f16_ta(d, a_lo + 8 * j, bd + 2 * j, C::kIdesc, j > 0 ? 1u : 0u);
+                // D = hi*W^T + 2^-10 * D, then the rest of hi*W^T
+                umma_f16_ta_scale10(d, a_hi, bd, C::kIdesc);
+#pragma unroll
+                for (int j = 1; j < BK / 16; ++j)
+                    umma_f16_ta(d, a_hi + 8 * j, bd + 2 * j, C::kIdesc, 1u);
+                umma_commit(&bars->wempty[sw]);
+                umma_commit(&bars->aempty[sa]);
+                umma_commit(&bars->dfull[b]);
             }
-            if (kb == num_kb) {
-                umma_commit(&bars->acc);
-            } else {
-                // aborted: wait for the MMAs already issued before TMEM is freed
+            if (!ok) {
                 umma_commit(&bars->drain);
-                const long long start = clock64();
-                while (!mbar_try_wait(&bars->drain, 0) && clock64() - start < kWaitLimit) {
-                }
+                drain_wait(&bars->drain, 0);
             }
         }
-        __syncwarp();
-    } else {
-        // ---------------- split, then epilogue ----------------
-        const int sw = warp - 2;                       // 0..3
-        const uint32_t row = static_cast<uint32_t>(sw * 32 + lane);  // split row, 0..127
-        bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t round = static_cast<uint32_t>(kb / kStages);
-            if (kTma) {
-                ok = wait_bounded(&bars->full[s], round & 1, bars, kFaultSplitFull);
-                ok = __all_sync(0xffffffffu, ok);  // uniform per warp
-            } else {
-                if (kb >= kStages)
-                    ok = wait_bounded(&bars->empty[s], (round - 1) & 1, bars, kFaultSplitEmpty);
-                if (__all_sync(0xffffffffu, ok))
-                    stage_plain(stage_w(s), stage_a(s), x, W, M, N, K, m0, n0, static_cast<int64_t>(kb) * BK, sw,
-                                lane);
-                ok = split_warps_all(ok);  // barrier over the split warps; uniform across them
-            }
-            if (!ok)
+    } else if (warp < 12) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPromoRegs));
+        // ---------------- promotion: R (+)= D per K block, then store y ----------------
+        const int wq = warp & 3;         // TMEM lane quarter this warp may access
+        const int wh = (warp - 4) >> 2;  // column half of the tile
+        float R[C::kHalf];
+        Cursor<BN> cur;
+        cur.start(P);
+        for (int j = 0; j < total; ++j, cur.next(P)) {
+            const int b = j & 1;
+            if (!warp_wait(&bars->dfull[b], (j >> 1) & 1, bars, kFaultPromote))
                 break;
-            split_row_inplace(stage_a(s), row);
-            fence_proxy_async_smem();
+            tc_fence_after();
+            const bool first = cur.kb == 0;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * BN + wh * C::kHalf;
+            uint32_t v[C::kHalf];  // the whole half row in one round trip
+#pragma unroll
+            for (int c = 0; c < C::kHalf; c += 16)
+                tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
+            tmem_ld_wait();
+            if (first) {
+#pragma unroll
+                for (int i = 0; i < C::kHalf; ++i)
+                    R[i] = __uint_as_float(v[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < C::kHalf; i += 2)
+                    add2(R[i], R[i + 1], v[i], v[i + 1]);
+            }
+            tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&bars->ready[s]);
-        }
+                mbar_arrive(&bars->dfree[b]);
 
-        if (ok)
-            ok = __all_sync(0xffffffffu, wait_bounded(&bars->acc, 0, bars, kFaultEpilogue));
-        if (ok) {
-            tc_fence_after();
-            const int q = warp & 3;  // TMEM lane quarter this warp may access
-            const int64_t m = m0 + q * 32 + lane;
-            const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
-#pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t rh[32], rl[32];
-                tmem_ld_32x32b_x32(t_lane + 32 * j, rh);
-                tmem_ld_32x32b_x32(t_lane + BN + 32 * j, rl);
-                tmem_ld_wait();
-                if (m < M) {
-                    const int64_t nb = n0 + 32 * j;
-                    float* yrow = y + m * N;
-                    float out[32];
+            if (cur.kb == P.nk - 1) {
+                // tile finished: R holds y[m, nb .. nb + BN/2) for this thread's row m
+                const int64_t m = static_cast<int64_t>(cur.m0) + wq * 32 + lane;
+                const int64_t nb = static_cast<int64_t>(cur.n0) + wh * C::kHalf;
+                if (m < P.M) {
+                    float* yrow = P.y + m * P.N;
+                    if (P.vec_y && nb + C::kHalf <= P.N) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        out[i] = __fadd_rn(__uint_as_float(rh[i]), __fmul_rn(__uint_as_float(rl[i]), 0x1p-10f));
-                    if (vec_y && nb + 32 <= N) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(yrow + nb + i) =
-                                make_float4(out[i], out[i + 1], out[i + 2], out[i + 3]);
+                        for (int i = 0; i < C::kHalf; i += 4)
+                            *reinterpret_cast<float4*>(yrow + nb + i) = make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (nb + i < N)
-                                yrow[nb + i] = out[i];
+                        for (int i = 0; i < C::kHalf; ++i)
+                            if (nb + i < P.N)
+                                yrow[nb + i] = R[i];
                     }
                 }
             }
+        }
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSplitRegs));
+        // ---------------- split: half a row of x -> hi/lo in tensor memory ----------------
+        const int q = warp & 3;               // TMEM lane quarter
+        const int kh = (warp - 12) >> 2;      // half of the K block: elements 32*kh .. 32*kh+31
+        const uint32_t row = q * 32 + lane;   // row of the tile this thread splits
+        const int st = threadIdx.x - 384;     // 0..255 (plain-path W staging)
+        const uint32_t xring_s = smem_u32(xring);
+        // byte offsets of this thread's 16-byte chunks of its row in an x box
+        uint32_t xoff[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            xoff[c] = sw128(row, c);
+        Cursor<BN> cur;
+        cur.start(P);
+        for (int g = 0; g < total; ++g, cur.next(P)) {
+            const int sx = g % kXStages;
+            const int sa = g % C::kAStages;
+            const int64_t k0 = static_cast<int64_t>(cur.kb) * BK;
+            if (kVec) {
+                if (!warp_wait(&bars->xfull[sx], (g / kXStages) & 1, bars, kFaultSplitX))
+                    break;
+            } else {
+                // plain path: stage the W box with bounds-checked loads (BN rows x 8 chunks of 8 FP16)
+                const int sw = g % kWStages;
+                if (g >= kWStages && !warp_wait(&bars->wempty[sw], ((g / kWStages) - 1) & 1, bars, kFaultSplitW))
+                    break;
+                const int64_t n0 = cur.n0;
+                uint8_t* Wt = wring + sw * C::kWBytes;
+#pragma unroll 1
+                for (int cid = st; cid < BN * 8; cid += 32 * kSplitters) {
+                    const int r = cid >> 3, c = cid & 7;
+                    const int64_t n = n0 + r;
+                    uint32_t h[4] = {0, 0, 0, 0};
+                    if (n < P.N) {
+                        const uint16_t* wrow = P.W + n * P.K;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int64_t k = k0 + 8 * c + e;
+                            const uint32_t v = k < P.K ? wrow[k] : 0u;
+                            h[e >> 1] |= v << (16 * (e & 1));
+                        }
+                    }
+                    *reinterpret_cast<uint4*>(Wt + sw128(r, c)) = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars->wfull[sw]);
+            }
+            if (g >= C::kAStages && !warp_wait(&bars->aempty[sa], ((g / C::kAStages) - 1) & 1, bars, kFaultSplitA))
+                break;
+            tc_fence_after();
+            const uint32_t X = xring_s + sx * kXBytes + kh * kXBox;
+            const int64_t m = static_cast<int64_t>(cur.m0) + row;
+            // TMEM columns of this thread's part: hi at 16*kh .., lo at 32 + 16*kh ..
+            const uint32_t a_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kACol + sa * 64 + 16 * kh;
+#pragma unroll
+            for (int qr = 0; qr < 2; ++qr) {  // 16 elements: k = 32*kh + 16*qr .. +15 -> 8 TMEM columns
+                float v[16];
+                if (kVec) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float4 f = lds128(X + xoff[4 * qr + c]);
+                        v[4 * c] = f.x;
+                        v[4 * c + 1] = f.y;
+                        v[4 * c + 2] = f.z;
+                        v[4 * c + 3] = f.w;
+                    }
+                } else {
+                    const float* xrow = P.x + (m < P.M ? m : 0) * static_cast<int64_t>(P.K);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int64_t k = k0 + 32 * kh + 16 * qr + e;
+                        v[e] = (m < P.M && k < P.K) ? __ldg(xrow + k) : 0.0f;
+                    }
+                }
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int p = 0; p < 8; ++p)
+                    split2(v[2 * p], v[2 * p + 1], hi[p], lo[p]);
+                tmem_st8(a_row + 8 * qr, hi);
+                tmem_st8(a_row + 32 + 8 * qr, lo);
+            }
+            tmem_st_wait();
+            if (kVec) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bars->xempty[sx]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->aready[sa]);
         }
     }
 
@@ -388,6 +620,8 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// A 2-D row-major tensor (inner extent `inner` contiguous, `outer` rows) as a
+// tensor map with box_inner x box_outer boxes and the 128-byte swizzle.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, size_t elem, const void* base, int64_t inner,
                int64_t outer, uint32_t box_inner, uint32_t box_outer)
 {
@@ -403,23 +637,49 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, size_t elem, const v
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kTma>
-bool configure_once(int device)
+template <int BN, bool kVec>
+comp_status_t launch_bn(const CUtensorMap& tw, const CUtensorMap& tx, const Problem& P, const DeviceInfo& dev,
+                        cudaStream_t stream)
 {
     static std::mutex mu;
     static bool done[64] = {};
-    std::lock_guard<std::mutex> lock(mu);
-    if (device < 0 || device >= 64)
-        return false;
-    if (!done[device]) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes)) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return false;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev.device < 0 || dev.device >= 64)
+            return COMP_ERR_CUDA;
+        if (!done[dev.device]) {
+            if (cudaFuncSetAttribute(comp_gemm_kernel<BN, kVec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(Cfg<BN>::kSmem)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return COMP_ERR_CUDA;
+            }
+            done[dev.device] = true;
         }
-        done[device] = true;
     }
-    return true;
+    const int tiles = P.tiles_m * P.tiles_n;
+    const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+    comp_gemm_kernel<BN, kVec><<<grid, kThreads, Cfg<BN>::kSmem, stream>>>(tw, tx, P);
+    return launch_status();
+}
+
+// The N tile width expected to finish first: rounds of tiles over the SMs
+// times the per-tile cost, modelled as BN plus a fixed 64 for the per-block
+// split and promotion work; ties go to the wider tile.
+int pick_bn(int64_t M, int64_t N, int sms)
+{
+    static const int cands[] = {160, 128};
+    int best = 128;
+    int64_t best_cost = INT64_MAX;
+    for (int bn : cands) {
+        const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+        const int64_t rounds = (tiles + sms - 1) / sms;
+        const int64_t cost = rounds * (bn + 64);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
 }
 
 inline bool aligned16(const void* p)
@@ -427,47 +687,52 @@ inline bool aligned16(const void* p)
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+template <bool kVec>
+comp_status_t dispatch(int bn, const CUtensorMap& tw, const CUtensorMap& tx, const Problem& P, const DeviceInfo& dev,
+                       cudaStream_t s)
+{
+    switch (bn) {
+    case 160:
+        return launch_bn<160, kVec>(tw, tx, P, dev, s);
+    default:
+        return launch_bn<128, kVec>(tw, tx, P, dev, s);
+    }
+}
+
 }  // namespace
 
 comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                              int variant, const DeviceInfo& dev, cudaStream_t stream)
 {
-    const bool tma_ok = aligned16(x) && aligned16(W) && (K % 8 == 0);
-    bool use_tma;
-    if (variant == 1) {
-        if (!tma_ok)
-            return COMP_ERR_INVALID_VALUE;
-        use_tma = true;
-    } else if (variant == 2) {
-        use_tma = false;
-    } else {
-        use_tma = tma_ok;
-    }
-    const int64_t grid_y = (M + BM - 1) / BM;
-    const int64_t grid_x = (N + BN - 1) / BN;
-    if (grid_y > 65535 || grid_x > 0x7FFFFFFF)
+    const bool vec_ok = aligned16(x) && aligned16(W) && (K % 8 == 0);
+    if (variant == 1 && !vec_ok)
         return COMP_ERR_INVALID_VALUE;
-    const int vec_y = (N % 4 == 0) && aligned16(y);
+    bool use_vec = variant == 2 ? false : vec_ok;
 
-    CUtensorMap tx{}, tw{};
-    if (use_tma && !(encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, K, M, 32, BM) &&
-                     encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, BN))) {
+    Problem P;
+    P.x = x;
+    P.W = W;
+    P.y = y;
+    P.M = static_cast<int>(M);
+    P.N = static_cast<int>(N);
+    P.K = static_cast<int>(K);
+    P.nk = static_cast<int>((K + BK - 1) / BK);
+    P.vec_y = (N % 4 == 0) && aligned16(y);
+    const int bn = pick_bn(M, N, dev.sm_count);
+    P.tiles_m = static_cast<int>((M + BM - 1) / BM);
+    P.tiles_n = static_cast<int>((N + bn - 1) / bn);
+    if (static_cast<int64_t>(P.tiles_m) * P.tiles_n > INT32_MAX / 2 ||
+        static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
+        return COMP_ERR_INVALID_VALUE;
+
+    CUtensorMap tw{}, tx{};
+    if (use_vec && !(encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn)) &&
+                     encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, K, M, 32, BM))) {
         if (variant == 1)
             return COMP_ERR_CUDA;
-        use_tma = false;  // the driver refused the descriptors: take the plain-load kernel
+        use_vec = false;  // the driver refused a descriptor: plain loads
     }
-    if (use_tma) {
-        if (!configure_once<true>(dev.device))
-            return COMP_ERR_CUDA;
-        gemm_tc_kernel<true><<<dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(grid_y)), kThreads,
-                               kSmemBytes, stream>>>(tx, tw, x, W, y, M, N, K, vec_y);
-    } else {
-        if (!configure_once<false>(dev.device))
-            return COMP_ERR_CUDA;
-        gemm_tc_kernel<false><<<dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(grid_y)), kThreads,
-                                kSmemBytes, stream>>>(tx, tw, x, W, y, M, N, K, vec_y);
-    }
-    return launch_status();
+    return use_vec ? dispatch<true>(bn, tw, tx, P, dev, stream) : dispatch<false>(bn, tw, tx, P, dev, stream);
 }
 
 comp_status_t read_and_clear_fault(cudaStream_t stream, uint32_t* where)
