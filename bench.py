@@ -1,0 +1,452 @@
+"""Benchmark of the compensated-FP32 projection on GB300.
+
+One step is one compensated projection y = x W^T of the 4096 x 4096 x 4096
+square shape (x FP32 ~ N(0,1), W FP16 ~ N(0,0.02)) through the fused kernel
+comp_gemm_f32x16, which performs the whole path: the split of x into FP16
+hi/lo, both tensor-core products and the FP32 merge.  The metric is effective
+FP32-GEMM throughput, 2*M*N*K per second.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: every step gets its own CUDA-event pair on the launching stream; the
+L2 cache (129 MB, larger than the 96 MB of inputs) is flushed by writing a
+256 MiB buffer before each step, outside the event pair.  The K timed steps
+are bracketed by a barrier and a device synchronisation on both sides, and
+the slowest rank's time is reported.  N > 1 runs one independent replica per
+GPU (the path has no exchange step), so scaling is weak.
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores
+on a bounded sample of the same workload: the pages give no GPU code for this
+path, so the oracle is the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "comp-FP32 GEMM effective TFLOPS (2MNK/s) & % of FP16 TC roofline; split GB/s"
+UNIT = "TFLOP/s"
+WORKLOAD = "square"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "comp_gemm_f32x16_square.md")
+KERNEL_SOURCE = os.path.join(ROOT, "compensated_fp32_projection_gb300", "csrc", "gemm_tc.cu")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sha():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def measured_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel source sha256") != kernel_sha():
+        return None
+    try:
+        return int(fields["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.reader = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_cpu_baseline(x, W, target_s: float = 12.0):
+    """The CPU oracle's compensated GEMM on the first rows of the workload, sized
+    for about `target_s` seconds of host work.  Returns effective TFLOP/s and a
+    description of the sample."""
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    xn = x.numpy()
+    wn = W.view(__import__("torch").int16).numpy().view(np.uint16)
+    M, K = xn.shape
+    N = wn.shape[0]
+    t0 = time.perf_counter()
+    oracle.gemm_comp(xn[:8], wn)  # calibration
+    dt = time.perf_counter() - t0
+    rows = int(min(M, max(8, 8 * target_s / max(dt, 1e-3))))
+    t0 = time.perf_counter()
+    oracle.gemm_comp(xn[:rows], wn)
+    dt = time.perf_counter() - t0
+    return {
+        "value": 2.0 * rows * N * K / dt / 1e12,
+        "unit": UNIT,
+        "cores": oracle.default_threads(),
+        "kind": "oracle",
+        "sample": f"first {rows} of {M} rows of the square shape (all {N} columns, full K={K}), FP64 sums, "
+                  f"{dt:.1f} s",
+    }
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, each step a bounded row sample."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from compensated_fp32_projection_gb300 import workloads
+
+    oracle.build()
+    s = workloads.SHAPES[WORKLOAD]
+    x, W = workloads.make_inputs(WORKLOAD)
+    xn = x.numpy()
+    wn = W.view(__import__("torch").int16).numpy().view(np.uint16)
+    # one output row per step (all N columns, full K), through the oracle's
+    # sampled mode: a bounded sample, so the whole run ends within minutes
+    cols = np.arange(s.N, dtype=np.int64)
+
+    def sample(i):
+        r = np.full(s.N, i % s.M, dtype=np.int64)
+        return oracle.gemm_comp(xn, wn, r, cols)
+
+    for i in range(args.warmup):
+        sample(i)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        sample(i)
+        times.append(time.perf_counter() - t0)
+    per_step = statistics.mean(times)
+    value = 2.0 * s.N * s.K / per_step / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} {s.M}x{s.N}x{s.K}, one output row per step (CPU oracle)",
+                   "M": s.M, "N": s.N, "K": s.K},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+                         "sample": f"1 row x {s.N} columns x K={s.K} per step (sampled mode), FP64 sums"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_kernel(fn, flush, stream, reps: int, warm: int = 3):
+    """Median and mean of per-launch CUDA-event times (ms), L2 flushed before each."""
+    import torch
+
+    for _ in range(warm):
+        flush.zero_()
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts), statistics.mean(ts)
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import compensated_fp32_projection_gb300 as pkg
+    from compensated_fp32_projection_gb300 import workloads
+
+    s = workloads.SHAPES[WORKLOAD]
+    x_cpu, W_cpu = workloads.make_inputs(WORKLOAD)
+    x = x_cpu.to(dev)
+    W = W_cpu.to(dev)
+    y = torch.empty((s.M, s.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkg.comp_gemm_f32x16(x, W, y)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    warm = max(3, args.warmup)
+    for _ in range(warm):
+        flush.zero_()
+        step()
+    barrier()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start
+    barrier()
+    events = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        events.append((a, b))
+    barrier()
+    clocks = sampler.stop()
+    times = [a.elapsed_time(b) for a, b in events]  # ms
+    ms = statistics.mean(times)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st, where = pkg.device_status()
+    if st != 0:
+        raise RuntimeError(f"kernel fault word {where:#x}")
+
+    flops = float(s.flops)
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    x_h = x_cpu.pin_memory()
+    W_h = W_cpu.pin_memory()
+    y_h = torch.empty((s.M, s.N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 30))
+    for _ in range(2):
+        x.copy_(x_h, non_blocking=True)
+        W.copy_(W_h, non_blocking=True)
+        pkg.comp_gemm_f32x16(x, W, y)
+        y_h.copy_(y, non_blocking=True)
+    barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(x_h, non_blocking=True)
+        W.copy_(W_h, non_blocking=True)
+        pkg.comp_gemm_f32x16(x, W, y)
+        y_h.copy_(y, non_blocking=True)
+    b.record(stream)
+    barrier()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peaks, peak_src = load_peaks()
+    tensor_flops = 2.0 * flops  # two FP16 products per effective FP32 multiply-add
+    achieved = tensor_flops / (statistics.mean(times) * 1e-3) / 1e12
+    traffic = measured_traffic()
+
+    # the standalone split and merge at the square shape's size (HBM bound), and the SIMT reference
+    n = s.M * s.K
+    xs = torch.randn(n, device=dev)
+    hi = torch.empty(n, dtype=torch.float16, device=dev)
+    lo = torch.empty(n, dtype=torch.float16, device=dev)
+    med, mean = time_kernel(lambda: pkg.comp_split_f32(xs, hi, lo), flush, stream, 20)
+    split_gbs = 8.0 * n / (mean * 1e-3) / 1e9
+    a32 = torch.randn(n, device=dev)
+    b32 = torch.randn(n, device=dev)
+    o32 = torch.empty(n, device=dev)
+    med, mean = time_kernel(lambda: pkg.comp_merge_f32(a32, b32, o32), flush, stream, 20)
+    merge_gbs = 12.0 * n / (mean * 1e-3) / 1e9
+    med, mean = time_kernel(lambda: pkg.comp_gemm_f32_simt(x, W, y), flush, stream, 3, warm=1)
+    simt_tflops = flops / (mean * 1e-3) / 1e12
+    del xs, hi, lo, a32, b32, o32
+
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_cpu_baseline(x_cpu, W_cpu)
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": warm,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{WORKLOAD} dense projection {s.M}x{s.N}x{s.K}: x FP32 N(0,1), W FP16 N(0,0.02) RNE, "
+                        f"y FP32; fused comp_gemm_f32x16 (split, two FP16 tensor-core products, FP32 merge)",
+            "M": s.M,
+            "N": s.N,
+            "K": s.K,
+            "seed": workloads.SEED_BASE + s.index,
+            "l2": "flushed before every timed step (256 MiB write, outside the event pair)",
+            "replicas": world,
+        },
+        "roofline": {
+            "bound": "tensor",
+            "achieved": achieved,
+            "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"],
+            "traffic": traffic,
+            "peak_source": f"{peak_src} dense bf16 burst (FP16 runs at the same tensor rate)",
+            "work": "4*M*N*K tensor FLOP per launch (hi and lo products)",
+            "effective_frac_of_roofline": value / world / (peaks["bf16_tflops"] / 2.0),
+        },
+        "e2e": {
+            "value": world * flops / (e2e_ms * 1e-3) / 1e12,
+            "unit": UNIT,
+            "h2d_bytes_per_step": 4 * s.M * s.K + 2 * s.N * s.K,
+            "d2h_bytes_per_step": 4 * s.M * s.N,
+        },
+        "gpu_launches": args.steps,
+        "kernels": {
+            "comp_split_f32": {"n": n, "GB/s": split_gbs, "frac_of_hbm": split_gbs / peaks["hbm_gbs"]},
+            "comp_merge_f32": {"n": n, "GB/s": merge_gbs, "frac_of_hbm": merge_gbs / peaks["hbm_gbs"]},
+            "comp_gemm_f32_simt": {"TFLOP/s": simt_tflops},
+        },
+    }
+    if clocks is not None:
+        line["clocks"] = clocks
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
