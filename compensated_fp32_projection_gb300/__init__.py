@@ -22,6 +22,9 @@ __all__ = [
     "comp_gemm_f32x16",
     "comp_gemm_f32x16_variant",
     "comp_gemm_f32_simt",
+    "comp_gemm_f16x2",
+    "comp_gemm_f32x16_ws",
+    "comp_gemm_workspace_bytes",
     "device_status",
     "status_string",
 ]
@@ -115,4 +118,46 @@ def comp_gemm_f32_simt(x, W, y=None, stream=None):
     """The true-FP32 reference product on the CUDA cores: y = x float(W)^T."""
     M, N, K, y = _gemm_args(x, W, y)
     _native.call("comp_gemm_f32_simt", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K, _stream(x, stream))
+    return y
+
+
+def comp_gemm_f16x2(hi, lo, W, y=None, stream=None):
+    """y = hi W^T + 2^-10 lo W^T from the split planes of comp_split_f32 (FP32 out)."""
+    torch = _torch()
+    _check(hi, torch.float16, "hi")
+    _check(lo, torch.float16, "lo")
+    _check(W, torch.float16, "W")
+    if hi.shape != lo.shape:
+        raise ValueError("hi and lo differ in shape")
+    if hi.dim() != 2 or W.dim() != 2 or hi.shape[1] != W.shape[1]:
+        raise ValueError("hi and lo must be [M, K] and W [N, K]")
+    M, K = hi.shape
+    N = W.shape[0]
+    y = torch.empty((M, N), dtype=torch.float32, device=hi.device) if y is None else y
+    _check(y, torch.float32, "y")
+    if tuple(y.shape) != (M, N):
+        raise ValueError("y must be [M, N]")
+    _native.call("comp_gemm_f16x2", hi.data_ptr(), lo.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K,
+                 _stream(hi, stream))
+    return y
+
+
+def comp_gemm_workspace_bytes(M, K):
+    """Workspace bytes the two-pass form of comp_gemm_f32x16_ws needs (4*M*K)."""
+    return int(_native.load().comp_gemm_workspace_bytes(int(M), int(K)))
+
+
+def comp_gemm_f32x16_ws(x, W, y=None, workspace=None, stream=None):
+    """comp_gemm_f32x16 with a device workspace (uint8 tensor); with enough room
+    (comp_gemm_workspace_bytes) it runs the two-pass form: split once, then the
+    two products and the merge."""
+    torch = _torch()
+    M, N, K, y = _gemm_args(x, W, y)
+    if workspace is None:
+        workspace = torch.empty(comp_gemm_workspace_bytes(M, K), dtype=torch.uint8, device=x.device)
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    _native.call("comp_gemm_f32x16_ws", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K, workspace.data_ptr(),
+                 nbytes, _stream(x, stream))
     return y

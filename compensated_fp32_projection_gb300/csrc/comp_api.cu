@@ -63,10 +63,11 @@ comp_status_t current_device(DeviceInfo* info)
 
 namespace {
 
-// Shared checks of the two GEMM entry points.  Sets *empty when there is
+// Shared checks of the GEMM entry points; x has x_elem bytes per element (4
+// for FP32 activations, 2 for one FP16 split plane).  Sets *empty when there is
 // nothing to launch (after writing y = 0 for K == 0).
-comp_status_t check_gemm(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
-                         cudaStream_t stream, DeviceInfo* dev, bool* empty)
+comp_status_t check_gemm(const void* x, int64_t x_elem, const uint16_t* W, float* y, int64_t M, int64_t N,
+                         int64_t K, cudaStream_t stream, DeviceInfo* dev, bool* empty)
 {
     *empty = false;
     int64_t mk, nk, mn;
@@ -82,7 +83,7 @@ comp_status_t check_gemm(const float* x, const uint16_t* W, float* y, int64_t M,
     }
     if (!y || (K > 0 && (!x || !W)))
         return COMP_ERR_INVALID_VALUE;
-    if (overlap(y, 4 * mn, x, 4 * mk) || overlap(y, 4 * mn, W, 2 * nk))
+    if (overlap(y, 4 * mn, x, x_elem * mk) || overlap(y, 4 * mn, W, 2 * nk))
         return COMP_ERR_INVALID_VALUE;
     const comp_status_t st = current_device(dev);
     if (st != COMP_OK)
@@ -143,7 +144,7 @@ comp_status_t comp_gemm_f32x16_variant(const float* x, const uint16_t* W, float*
     DeviceInfo dev;
     bool empty;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const comp_status_t st = check_gemm(x, W, y, M, N, K, s, &dev, &empty);
+    const comp_status_t st = check_gemm(x, 4, W, y, M, N, K, s, &dev, &empty);
     if (st != COMP_OK || empty)
         return st;
     return launch_gemm_tc(x, W, y, M, N, K, variant, dev, s);
@@ -161,10 +162,63 @@ comp_status_t comp_gemm_f32_simt(const float* x, const uint16_t* W, float* y, in
     DeviceInfo dev;
     bool empty;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const comp_status_t st = check_gemm(x, W, y, M, N, K, s, &dev, &empty);
+    const comp_status_t st = check_gemm(x, 4, W, y, M, N, K, s, &dev, &empty);
     if (st != COMP_OK || empty)
         return st;
     return launch_gemm_simt(x, W, y, M, N, K, dev, s);
+}
+
+comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
+                              int64_t N, int64_t K, comp_stream_t stream)
+{
+    DeviceInfo dev;
+    bool empty;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const comp_status_t st = check_gemm(hi, 2, W, y, M, N, K, s, &dev, &empty);
+    if (st != COMP_OK || empty)
+        return st;
+    // check_gemm has bounded M*N and M*K
+    if (!lo || overlap(y, 4 * M * N, lo, 2 * M * K))
+        return COMP_ERR_INVALID_VALUE;
+    if (!gemm_f16x2_supported(hi, lo, W, K))
+        return COMP_ERR_INVALID_VALUE;
+    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, dev, s);
+}
+
+int64_t comp_gemm_workspace_bytes(int64_t M, int64_t K)
+{
+    int64_t mk = 0;
+    if (!mul_ok(M, K, &mk) || mk > INT64_MAX / 4)
+        return 0;
+    return 4 * mk;
+}
+
+comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                                  void* workspace, int64_t workspace_bytes, comp_stream_t stream)
+{
+    DeviceInfo dev;
+    bool empty;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const comp_status_t st = check_gemm(x, 4, W, y, M, N, K, s, &dev, &empty);
+    if (st != COMP_OK || empty)
+        return st;
+    const int64_t need = comp_gemm_workspace_bytes(M, K);
+    if (workspace_bytes < 0 || (workspace_bytes > 0 && !workspace))
+        return COMP_ERR_INVALID_VALUE;
+    if (workspace && workspace_bytes > 0 &&
+        (overlap(workspace, workspace_bytes, x, 4 * M * K) || overlap(workspace, workspace_bytes, W, 2 * N * K) ||
+         overlap(workspace, workspace_bytes, y, 4 * M * N)))
+        return COMP_ERR_INVALID_VALUE;
+    uint16_t* hi = static_cast<uint16_t*>(workspace);
+    uint16_t* lo = hi ? hi + M * K : nullptr;
+    const bool two_pass = workspace && need > 0 && workspace_bytes >= need &&
+                          (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && gemm_f16x2_supported(hi, lo, W, K);
+    if (!two_pass)
+        return launch_gemm_tc(x, W, y, M, N, K, 0, dev, s);
+    const comp_status_t sp = launch_split(x, hi, lo, M * K, dev, s);
+    if (sp != COMP_OK)
+        return sp;
+    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, dev, s);
 }
 
 comp_status_t comp_device_status(comp_stream_t stream, uint32_t* where)

@@ -115,7 +115,7 @@ struct Barriers {
     int abort;
 };
 
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Barriers* b, uint32_t code)
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int* abort_flag, uint32_t code)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -123,11 +123,11 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Bar
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 20000))
             return true;
-        if (*reinterpret_cast<volatile int*>(&b->abort))
+        if (*reinterpret_cast<volatile int*>(abort_flag))
             return false;
         if (clock64() - start > kWaitLimit) {
             atomicCAS(&g_fault_word, 0u, code);
-            *reinterpret_cast<volatile int*>(&b->abort) = 1;
+            *reinterpret_cast<volatile int*>(abort_flag) = 1;
             return false;
         }
     }
@@ -136,11 +136,11 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Bar
 // Warp-wide bounded wait: lane 0 polls, the verdict is broadcast, and on
 // success every lane performs one (immediately successful) try_wait so that it
 // observes the phase completion itself.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Barriers* b, uint32_t code)
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* abort_flag, uint32_t code)
 {
     bool ok = true;
     if ((threadIdx.x & 31) == 0)
-        ok = wait_bounded(bar, parity, b, code);
+        ok = wait_bounded(bar, parity, abort_flag, code);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (ok)
         (void)mbar_try_wait(bar, parity);
@@ -273,6 +273,17 @@ __device__ __forceinline__ void umma_f16_ta_scale10(uint32_t d_tmem, uint32_t a_
         : "memory");
 }
 
+// D = A * B^T + D * 2^-10 with A and B in shared memory.
+__device__ __forceinline__ void umma_f16_ss_scale10(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, 1, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p, 10;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc)
+        : "memory");
+}
+
 struct Problem {
     const float* x;
     const uint16_t* W;
@@ -384,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int g = 0; g < total; ++g, cur.next(P)) {
                 const int s = g % depth;
                 if (g >= depth &&
-                    !wait_bounded(&empty[s], ((g / depth) - 1) & 1, bars, is_w ? kFaultWProducer : kFaultXProducer))
+                    !wait_bounded(&empty[s], ((g / depth) - 1) & 1, &bars->abort, is_w ? kFaultWProducer : kFaultXProducer))
                     break;
                 const int k0 = cur.kb * BK;
                 if (is_w) {
@@ -411,9 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int sw = g % kWStages;
                 const int sa = g % C::kAStages;  // A stage
                 const int b = g & 1;          // accumulator buffer
-                ok = wait_bounded(&bars->wfull[sw], (g / kWStages) & 1, bars, kFaultMmaW) &&
-                     wait_bounded(&bars->aready[sa], (g / C::kAStages) & 1, bars, kFaultMmaA) &&
-                     (g < 2 || wait_bounded(&bars->dfree[b], ((g >> 1) - 1) & 1, bars, kFaultMmaD));
+                ok = wait_bounded(&bars->wfull[sw], (g / kWStages) & 1, &bars->abort, kFaultMmaW) &&
+                     wait_bounded(&bars->aready[sa], (g / C::kAStages) & 1, &bars->abort, kFaultMmaA) &&
+                     (g < 2 || wait_bounded(&bars->dfree[b], ((g >> 1) - 1) & 1, &bars->abort, kFaultMmaD));
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -444,29 +455,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wq = warp & 3;         // TMEM lane quarter this warp may access
         const int wh = (warp - 4) >> 2;  // column half of the tile
         float R[C::kHalf];
+#pragma unroll
+        for (int i = 0; i < C::kHalf; ++i)
+            R[i] = 0.0f;
         Cursor<BN> cur;
         cur.start(P);
         for (int j = 0; j < total; ++j, cur.next(P)) {
             const int b = j & 1;
-            if (!warp_wait(&bars->dfull[b], (j >> 1) & 1, bars, kFaultPromote))
+            if (!warp_wait(&bars->dfull[b], (j >> 1) & 1, &bars->abort, kFaultPromote))
                 break;
             tc_fence_after();
-            const bool first = cur.kb == 0;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * BN + wh * C::kHalf;
             uint32_t v[C::kHalf];  // the whole half row in one round trip
 #pragma unroll
             for (int c = 0; c < C::kHalf; c += 16)
                 tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
             tmem_ld_wait();
-            if (first) {
 #pragma unroll
-                for (int i = 0; i < C::kHalf; ++i)
-                    R[i] = __uint_as_float(v[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < C::kHalf; i += 2)
-                    add2(R[i], R[i + 1], v[i], v[i + 1]);
-            }
+            for (int i = 0; i < C::kHalf; i += 2)
+                add2(R[i], R[i + 1], v[i], v[i + 1]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
@@ -489,6 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 yrow[nb + i] = R[i];
                     }
                 }
+#pragma unroll
+                for (int i = 0; i < C::kHalf; ++i)
+                    R[i] = 0.0f;  // the next tile starts from +0 (0 + D = D exactly, except -0 -> +0)
             }
         }
     } else {
@@ -511,12 +521,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sa = g % C::kAStages;
             const int64_t k0 = static_cast<int64_t>(cur.kb) * BK;
             if (kVec) {
-                if (!warp_wait(&bars->xfull[sx], (g / kXStages) & 1, bars, kFaultSplitX))
+                if (!warp_wait(&bars->xfull[sx], (g / kXStages) & 1, &bars->abort, kFaultSplitX))
                     break;
             } else {
                 // plain path: stage the W box with bounds-checked loads (BN rows x 8 chunks of 8 FP16)
                 const int sw = g % kWStages;
-                if (g >= kWStages && !warp_wait(&bars->wempty[sw], ((g / kWStages) - 1) & 1, bars, kFaultSplitW))
+                if (g >= kWStages && !warp_wait(&bars->wempty[sw], ((g / kWStages) - 1) & 1, &bars->abort, kFaultSplitW))
                     break;
                 const int64_t n0 = cur.n0;
                 uint8_t* Wt = wring + sw * C::kWBytes;
@@ -541,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0)
                     mbar_arrive(&bars->wfull[sw]);
             }
-            if (g >= C::kAStages && !warp_wait(&bars->aempty[sa], ((g / C::kAStages) - 1) & 1, bars, kFaultSplitA))
+            if (g >= C::kAStages && !warp_wait(&bars->aempty[sa], ((g / C::kAStages) - 1) & 1, &bars->abort, kFaultSplitA))
                 break;
             tc_fence_after();
             const uint32_t X = xring_s + sx * kXBytes + kh * kXBox;
@@ -585,6 +595,243 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars->aready[sa]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The two products and the merge from split planes (comp_gemm_f16x2): the
+// second half of the two-pass form, in which comp_split_f32 writes hi and lo
+// once and this kernel reads both planes by TMA, so no split work is repeated
+// per output tile.  Per 128 x BN tile and chunk of two K blocks of 64:
+//   lo*W^T of both blocks into a fresh TMEM accumulator, then hi*W^T of both
+//   blocks, the first of which scales the accumulator by 2^-10 on input:
+//   D = hi*W^T + 2^-10 (lo*W^T) over the chunk; eight promotion warps add each
+//   chunk's D into FP32 registers (one FP32 addition per 128 of K).
+// ---------------------------------------------------------------------------
+namespace x2 {
+constexpr int kPromoters = 8;
+constexpr int kThreads = 128 + 32 * kPromoters;  // warpgroup 0: producer, MMA issuer, two idle warps
+// 384 threads launch with 168 registers each (pool 64512): control 40,
+// promotion 232: 128*40 + 256*232 = 64512.  The build checks the 168.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 40;
+constexpr int kPromoRegs = 232;
+static_assert(128 * kCtrlRegs + 32 * kPromoters * kPromoRegs <= kThreads * kLaunchRegs, "register split");
+constexpr int kStages = 4;
+constexpr uint32_t kPlaneBytes = BM * BK * 2;  // 16 KB: a 128 x 64 FP16 box
+
+template <int BN>
+struct Cfg {
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+    static constexpr uint32_t kWBytes = BN * BK * 2;
+    static constexpr uint32_t kStageBytes = 2 * kPlaneBytes + kWBytes;  // hi | lo | W
+    static constexpr size_t kSmem = 1024 + kStages * kStageBytes + 256;
+    static_assert(kSmem <= 232448, "shared memory");
+    static constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
+    static constexpr int kHalf = BN / 2;
+};
+
+struct Barriers {
+    uint64_t full[kStages];   // hi, lo and W boxes landed (TMA bytes)
+    uint64_t empty[kStages];  // MMAs reading the stage completed
+    uint64_t dfull[2];        // accumulator buffer holds a finished chunk
+    uint64_t dfree[2];        // promotion warps have read the accumulator buffer
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+}  // namespace x2
+
+// Fault codes of the two-pass product kernel.
+constexpr uint32_t kFaultX2Producer = 0x501;
+constexpr uint32_t kFaultX2MmaFull = 0x502;
+constexpr uint32_t kFaultX2MmaFree = 0x503;
+constexpr uint32_t kFaultX2Promote = 0x504;
+
+template <int BN>
+__global__ void __launch_bounds__(x2::kThreads, 1)
+    comp_f16x2_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
+                      const __grid_constant__ CUtensorMap tmap_w, const Problem P)
+{
+    using C = x2::Cfg<BN>;
+    constexpr int NS = x2::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    x2::Barriers* bars = reinterpret_cast<x2::Barriers*>(smem + NS * C::kStageBytes);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int num_tiles = P.tiles_m * P.tiles_n;
+    const int my_tiles =
+        static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const int total = my_tiles * P.nk;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->dfull[b], 1);
+            mbar_init(&bars->dfree[b], x2::kPromoters);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmap_hi);
+        tma_prefetch_desc(&tmap_lo);
+        tma_prefetch_desc(&tmap_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(x2::kCtrlRegs));
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer: hi, lo and W boxes per K block ----------------
+            int issued = 0;
+            Cursor<BN> cur;
+            cur.start(P);
+            for (int g = 0; g < total; ++g, cur.next(P)) {
+                const int s = g % NS;
+                if (g >= NS && !wait_bounded(&bars->empty[s], ((g / NS) - 1) & 1, &bars->abort, kFaultX2Producer))
+                    break;
+                uint8_t* st = smem + s * C::kStageBytes;
+                const int k0 = cur.kb * BK;
+                mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
+                tma_load_2d(st, &tmap_hi, &bars->full[s], k0, cur.m0);
+                tma_load_2d(st + x2::kPlaneBytes, &tmap_lo, &bars->full[s], k0, cur.m0);
+                tma_load_2d(st + 2 * x2::kPlaneBytes, &tmap_w, &bars->full[s], k0, cur.n0);
+                issued = g + 1;
+            }
+            if (*reinterpret_cast<volatile int*>(&bars->abort))
+                for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
+                    drain_wait(&bars->full[g % NS], (g / NS) & 1);
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- MMA issuer, one chunk (one or two K blocks) at a time ----------------
+            const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
+            bool ok = true;
+            int g = 0, c = 0, kb = 0;
+            while (g < total && ok) {
+                const int n = (kb + 1 < P.nk) ? 2 : 1;  // blocks in this chunk (chunks stay inside a tile)
+                const int b = c & 1;
+                for (int i = 0; i < n && ok; ++i)
+                    ok = wait_bounded(&bars->full[(g + i) % NS], ((g + i) / NS) & 1, &bars->abort, kFaultX2MmaFull);
+                if (ok && c >= 2)
+                    ok = wait_bounded(&bars->dfree[b], ((c >> 1) - 1) & 1, &bars->abort, kFaultX2MmaFree);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + b * BN;
+                // descriptor of stage s: hi at +0, lo at +16 KB, W at +32 KB (start field counts 16 bytes)
+                auto sdesc = [&](int blk, uint32_t off) {
+                    return desc0 + static_cast<uint64_t>(((blk % NS) * C::kStageBytes + off) >> 4);
+                };
+                for (int i = 0; i < n; ++i) {  // lo * W^T of the chunk; the very first overwrites D
+                    const uint64_t a = sdesc(g + i, x2::kPlaneBytes), w = sdesc(g + i, 2 * x2::kPlaneBytes);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)
+                        umma_f16(d, a + 2 * j, w + 2 * j, C::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+                }
+                for (int i = 0; i < n; ++i) {  // hi * W^T; the first scales D by 2^-10 on input
+                    const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * x2::kPlaneBytes);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j) {
+                        if (i == 0 && j == 0)
+                            umma_f16_ss_scale10(d, a, w, C::kIdesc);
+                        else
+                            umma_f16(d, a + 2 * j, w + 2 * j, C::kIdesc, 1u);
+                    }
+                    umma_commit(&bars->empty[(g + i) % NS]);
+                }
+                umma_commit(&bars->dfull[b]);
+                g += n;
+                ++c;
+                kb += n;
+                if (kb == P.nk)
+                    kb = 0;
+            }
+            if (!ok) {
+                umma_commit(&bars->drain);
+                drain_wait(&bars->drain, 0);
+            }
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(x2::kPromoRegs));
+        // ---------------- promotion: R += D per chunk, then store y ----------------
+        const int wq = warp & 3;         // TMEM lane quarter
+        const int wh = (warp - 4) >> 2;  // column half of the tile
+        float R[C::kHalf];
+#pragma unroll
+        for (int i = 0; i < C::kHalf; ++i)
+            R[i] = 0.0f;
+        int g = 0, c = 0, kb = 0;
+        int t = static_cast<int>(blockIdx.x);
+        while (g < total) {
+            const int n = (kb + 1 < P.nk) ? 2 : 1;
+            const int b = c & 1;
+            if (!warp_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultX2Promote))
+                break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * BN + wh * C::kHalf;
+#pragma unroll
+            for (int c0 = 0; c0 < C::kHalf; c0 += 64) {  // up to 64 columns per round trip
+                uint32_t v[64];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (c0 + 16 * q < C::kHalf)
+                        tmem_ld16(taddr + c0 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 64; i += 2)
+                    if (c0 + i < C::kHalf)
+                        add2(R[c0 + i], R[c0 + i + 1], v[i], v[i + 1]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->dfree[b]);
+            g += n;
+            ++c;
+            kb += n;
+            if (kb == P.nk) {
+                // tile finished: R holds y[m, nb .. nb + BN/2) for this thread's row m
+                const int64_t m = static_cast<int64_t>(tile_m(t, P)) * BM + wq * 32 + lane;
+                const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
+                if (m < P.M) {
+                    float* yrow = P.y + m * P.N;
+                    if (P.vec_y && nb + C::kHalf <= P.N) {
+#pragma unroll
+                        for (int i = 0; i < C::kHalf; i += 4)
+                            *reinterpret_cast<float4*>(yrow + nb + i) = make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < C::kHalf; ++i)
+                            if (nb + i < P.N)
+                                yrow[nb + i] = R[i];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < C::kHalf; ++i)
+                    R[i] = 0.0f;
+                kb = 0;
+                t += static_cast<int>(gridDim.x);
+            }
         }
     }
 
@@ -733,6 +980,84 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
         use_vec = false;  // the driver refused a descriptor: plain loads
     }
     return use_vec ? dispatch<true>(bn, tw, tx, P, dev, stream) : dispatch<false>(bn, tw, tx, P, dev, stream);
+}
+
+namespace {
+
+template <int BN>
+comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+                           const DeviceInfo& dev, cudaStream_t stream)
+{
+    static std::mutex mu;
+    static bool done[64] = {};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev.device < 0 || dev.device >= 64)
+            return COMP_ERR_CUDA;
+        if (!done[dev.device]) {
+            if (cudaFuncSetAttribute(comp_f16x2_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(x2::Cfg<BN>::kSmem)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return COMP_ERR_CUDA;
+            }
+            done[dev.device] = true;
+        }
+    }
+    const int tiles = P.tiles_m * P.tiles_n;
+    const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+    comp_f16x2_kernel<BN><<<grid, x2::kThreads, x2::Cfg<BN>::kSmem, stream>>>(th, tl, tw, P);
+    return launch_status();
+}
+
+// N tile width for the two-pass product (tiles are all tensor work there).
+int pick_bn_x2(int64_t M, int64_t N, int sms)
+{
+    static const int cands[] = {192, 128};
+    int best = 128;
+    int64_t best_cost = INT64_MAX;
+    for (int bn : cands) {
+        const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+        const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 32);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t K)
+{
+    return aligned16(hi) && aligned16(lo) && aligned16(W) && (K % 8 == 0);
+}
+
+comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
+                                int64_t N, int64_t K, const DeviceInfo& dev, cudaStream_t stream)
+{
+    if (!gemm_f16x2_supported(hi, lo, W, K))
+        return COMP_ERR_INVALID_VALUE;
+    Problem P;
+    P.x = nullptr;
+    P.W = W;
+    P.y = y;
+    P.M = static_cast<int>(M);
+    P.N = static_cast<int>(N);
+    P.K = static_cast<int>(K);
+    P.nk = static_cast<int>((K + BK - 1) / BK);
+    P.vec_y = (N % 4 == 0) && aligned16(y);
+    const int bn = pick_bn_x2(M, N, dev.sm_count);
+    P.tiles_m = static_cast<int>((M + BM - 1) / BM);
+    P.tiles_n = static_cast<int>((N + bn - 1) / bn);
+    if (static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
+        return COMP_ERR_INVALID_VALUE;
+    CUtensorMap th{}, tl{}, tw{};
+    if (!encode_2d(&th, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hi, K, M, BK, BM) ||
+        !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, BM) ||
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn)))
+        return COMP_ERR_CUDA;
+    return bn == 192 ? launch_x2_bn<192>(th, tl, tw, P, dev, stream) : launch_x2_bn<128>(th, tl, tw, P, dev, stream);
 }
 
 comp_status_t read_and_clear_fault(cudaStream_t stream, uint32_t* where)

@@ -28,6 +28,12 @@ comp_status_t launch_gemm_simt(const float* x, const uint16_t* W, float* y, int6
 comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                              int variant, const DeviceInfo& dev, cudaStream_t stream);
 
+// The two products and the merge from split planes (hi, lo: [M, K] FP16).
+// Needs 16-byte aligned hi, lo, W and K % 8 == 0 (else COMP_ERR_INVALID_VALUE).
+bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t K);
+comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
+                                int64_t N, int64_t K, const DeviceInfo& dev, cudaStream_t stream);
+
 // Reads and clears the fault word of the tensor-core kernels (after the stream
 // has been synchronised).
 comp_status_t read_and_clear_fault(cudaStream_t stream, uint32_t* where);

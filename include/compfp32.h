@@ -128,6 +128,45 @@ comp_status_t comp_gemm_f32x16_variant(const float* x, const uint16_t* W, float*
                                        int64_t K, int variant, comp_stream_t stream);
 
 /*
+ * comp_gemm_f16x2 — the two products and the merge, from the split planes
+ * (laya.cpp docs/vulkan.md, compensated-FP32 paragraph: both FP16 components
+ * multiplied by the exact FP16 weights with FP32 accumulators, combined in
+ * FP32; the split/merge paragraph: the split as its own dispatch).  Together
+ * with comp_split_f32 this is the two-pass form of comp_gemm_f32x16: the split
+ * runs once per element instead of once per output tile.
+ *   hi, lo : [M, K] binary16 planes as written by comp_split_f32 (input).
+ *   W      : [N, K] binary16 (input).   y : [M, N] binary32 (output).
+ *   y[m,n] = sum_k hi*W + 2^-10 * sum_k lo*W, FP32 accumulation on the tensor
+ *   cores (fresh per 128 of K, those partial sums added in FP32); same
+ *   tolerance as comp_gemm_f32x16.
+ * hi, lo and W must be 16-byte aligned and K a multiple of 8 (the tensor
+ * memory accelerator's layout rules), else COMP_ERR_INVALID_VALUE; also the
+ * errors of comp_gemm_f32x16 (y may not overlap an input).
+ */
+comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
+                              int64_t N, int64_t K, comp_stream_t stream);
+
+/*
+ * comp_gemm_workspace_bytes — the workspace comp_gemm_f32x16_ws needs for the
+ * two-pass form: 4 * M * K bytes (the hi and lo planes).  0 for a negative or
+ * overflowing size.
+ */
+int64_t comp_gemm_workspace_bytes(int64_t M, int64_t K);
+
+/*
+ * comp_gemm_f32x16_ws — comp_gemm_f32x16 with a caller-provided device
+ * workspace.  When the workspace holds comp_gemm_workspace_bytes(M, K) bytes,
+ * is 16-byte aligned, x and W are 16-byte aligned and K is a multiple of 8, the
+ * call enqueues the two-pass form: comp_split_f32 of x into the workspace (hi
+ * plane, then lo plane) and comp_gemm_f16x2.  Otherwise it is exactly
+ * comp_gemm_f32x16.  The workspace's contents are overwritten; it must not
+ * overlap x, W or y (COMP_ERR_INVALID_VALUE).  Same results within the same
+ * tolerance either way.
+ */
+comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                                  void* workspace, int64_t workspace_bytes, comp_stream_t stream);
+
+/*
  * comp_device_status — waits for `stream`, then reports and clears the fault
  * word that kernels of this library set when a bounded wait inside them gives
  * up (they then skip the rest of their work and exit cleanly, leaving the

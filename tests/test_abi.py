@@ -84,6 +84,26 @@ def test_gemm_argument_errors(lib):
     assert lib.comp_gemm_f32x16_variant(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, 7, None) == 1
 
 
+def test_two_pass_argument_errors(lib):
+    f2, ws = lib.comp_gemm_f16x2, lib.comp_gemm_f32x16_ws
+    # comp_gemm_f16x2(hi, lo, W, y, M, N, K, stream)
+    assert f2(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), -1, 4, 8, None) == 1
+    assert f2(None, P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, None) == 1
+    assert f2(P(4096), P(1 << 16), P(1 << 20), P(4096 + 32), 4, 4, 8, None) == 1  # y overlaps hi
+    assert f2(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 1 << 40, 1 << 40, 8, None) == 1
+    assert f2(None, None, None, None, 0, 4, 8, None) == 0
+    # comp_gemm_f32x16_ws(x, W, y, M, N, K, workspace, bytes, stream)
+    assert ws(P(4096), P(1 << 20), P(1 << 24), -1, 4, 4, P(1 << 26), 64, None) == 1
+    assert ws(None, None, None, 0, 4, 4, None, 0, None) == 0
+
+
+def test_workspace_bytes(lib):
+    assert lib.comp_gemm_workspace_bytes(4096, 4096) == 4 * 4096 * 4096
+    assert lib.comp_gemm_workspace_bytes(0, 77) == 0
+    assert lib.comp_gemm_workspace_bytes(-1, 8) == 0
+    assert lib.comp_gemm_workspace_bytes(1 << 40, 1 << 30) == 0  # overflows
+
+
 def test_no_device_is_an_error_not_a_fallback(lib):
     import torch
 
@@ -92,6 +112,8 @@ def test_no_device_is_an_error_not_a_fallback(lib):
     # valid arguments on a host without a usable sm_103 device: an error, never a CPU path
     assert lib.comp_split_f32(P(4096), P(1 << 20), P(1 << 21), 8, None) == 2
     assert lib.comp_gemm_f32x16(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, None) == 2
+    assert lib.comp_gemm_f16x2(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, None) == 2
+    assert lib.comp_gemm_f32x16_ws(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, P(1 << 26), 64, None) == 2
 
 
 def test_package_import_does_not_need_the_library():

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-TOL = 4e-6
+from gemm_check import check_comp, sample_outputs, w_bits  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -30,32 +30,6 @@ def pkg():
 
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     return p
-
-
-def w_bits(W):
-    return W.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-
-
-def check_comp(y, x, W, orc, rows=None, cols=None):
-    """Elementwise gate against the oracle; returns (gpu error, cast error) max-normalised vs the true product."""
-    xn, wn = x.cpu().numpy(), w_bits(W)
-    yg = y.detach().cpu().numpy()
-    if rows is not None:
-        yg = yg[rows, cols]
-    y_or = orc.gemm_comp(xn, wn, rows, cols).astype(np.float64)
-    den = orc.gemm_den(xn, wn, rows, cols)
-    err = np.abs(yg.astype(np.float64) - y_or)
-    bound = TOL * den + 1e-30
-    bad = np.argwhere(~(err <= bound))
-    assert bad.size == 0, (
-        f"{bad.shape[0]} elements over tolerance; first {bad[:3].tolist()}, "
-        f"worst ratio {float(np.nanmax(err / bound))}"
-    )
-    y_true = orc.gemm_true(xn, wn, rows, cols).astype(np.float64)
-    y_cast = orc.gemm_cast(xn, wn, rows, cols).astype(np.float64)
-    e_gpu = float(np.max(np.abs(yg - y_true) / (den + 1e-30)))
-    e_cast = float(np.max(np.abs(y_cast - y_true) / (den + 1e-30)))
-    return e_gpu, e_cast
 
 
 def gemm(pkg, x, W, variant):
@@ -80,13 +54,8 @@ def test_projection_shapes_sampled(pkg, orc, name):
 
     x, W = workloads.make_inputs(name)
     y = pkg.comp_gemm_f32x16(x.cuda(), W.cuda())
-    M, N = x.shape[0], W.shape[0]
-    rng = np.random.default_rng(5)
-    # random samples plus the corners and edges of the output
-    r = np.concatenate([rng.integers(0, M, 3000), [0, 0, M - 1, M - 1], np.full(16, M - 1), np.arange(min(M, 16))])
-    c = np.concatenate([rng.integers(0, N, 3000), [0, N - 1, 0, N - 1], np.arange(N - 16, N), np.full(min(M, 16), N - 1)])
-    order = np.argsort(r, kind="stable")
-    e_gpu, e_cast = check_comp(y, x, W, orc, r[order], c[order])
+    r, c = sample_outputs(x.shape[0], W.shape[0])
+    e_gpu, e_cast = check_comp(y, x, W, orc, r, c)
     assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
     assert torch.isfinite(y).all()
 

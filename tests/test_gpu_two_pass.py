@@ -1,0 +1,221 @@
+"""GPU parity of the two-pass compensated projection: the split as its own
+dispatch (laya.cpp docs/vulkan.md, split/merge paragraph) followed by the two
+FP16 products and the merge (compensated-FP32 paragraph), through
+comp_gemm_f32x16_ws and comp_gemm_f16x2.  Same gate as the fused kernel:
+elementwise within 4e-6 * sum|x||w| of the oracle and 100x more accurate than
+a single FP16 cast of x.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+from gemm_check import check_comp, sample_outputs  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import compensated_fp32_projection_gb300 as p
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return p
+
+
+def bits(t):
+    return t.contiguous().view(torch.int32)
+
+
+@pytest.mark.parametrize("name", ["tiny", "encoder"])
+def test_shapes_full(pkg, orc, name):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs(name)
+    y = pkg.comp_gemm_f32x16_ws(x.cuda(), W.cuda())
+    e_gpu, e_cast = check_comp(y, x, W, orc)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+
+
+@pytest.mark.parametrize("name", ["square", "skinny"])
+def test_shapes_sampled(pkg, orc, name):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs(name)
+    y = pkg.comp_gemm_f32x16_ws(x.cuda(), W.cuda())
+    r, c = sample_outputs(x.shape[0], W.shape[0])
+    e_gpu, e_cast = check_comp(y, x, W, orc, r, c)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+    assert torch.isfinite(y).all()
+
+
+def test_nonaligned_k_takes_the_fused_kernel(pkg, orc):
+    # K = 1027 is not a multiple of 8: the workspace is ignored and the result
+    # is the fused kernel's, bit for bit
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs("nonaligned")
+    x, W = x.cuda(), W.cuda()
+    y_ws = pkg.comp_gemm_f32x16_ws(x, W)
+    y_fused = pkg.comp_gemm_f32x16(x, W)
+    assert torch.equal(bits(y_ws), bits(y_fused))
+    check_comp(y_ws, x.cpu(), W.cpu(), orc)
+
+
+# K multiples of 8 only (the planes are read with the tensor memory accelerator);
+# ragged M, N and K tails, one and several 128-row / 128..192-column tiles, an
+# odd count of 64-wide K blocks, and K below one block
+SHAPES = [
+    (1, 1, 8),
+    (3, 5, 16),
+    (8, 384, 256),
+    (128, 256, 64),
+    (130, 300, 72),
+    (257, 513, 200),
+    (129, 257, 1032),
+    (200, 1000, 520),
+    (17, 260, 4096),
+    (384, 768, 24),
+    (1000, 771, 1024),
+    (640, 1152, 192),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tiles_and_ragged_tails(pkg, orc, shape):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=M * 1_000_003 + N * 101 + K + 7, scale=3.0)
+    y = pkg.comp_gemm_f32x16_ws(x.cuda(), W.cuda())
+    check_comp(y, x, W, orc)
+
+
+def test_f16x2_from_split_planes_equals_ws(pkg, orc):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.random_case(300, 520, 264, seed=19)
+    x, W = x.cuda(), W.cuda()
+    hi, lo = pkg.comp_split_f32(x)
+    y1 = pkg.comp_gemm_f16x2(hi, lo, W)
+    y2 = pkg.comp_gemm_f32x16_ws(x, W)
+    assert torch.equal(bits(y1), bits(y2))
+    check_comp(y1, x.cpu(), W.cpu(), orc)
+
+
+def test_hi_only_is_a_plain_fp16_product(pkg, orc):
+    # x exact in FP16: lo = 0 and y is the FP16 product with FP32 accumulation
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.random_case(256, 512, 512, seed=3)
+    x = x.half().float()
+    y = pkg.comp_gemm_f32x16_ws(x.cuda(), W.cuda())
+    check_comp(y, x, W, orc)
+    hi, lo = pkg.comp_split_f32(x.cuda())
+    assert not lo.view(torch.int16).any()
+
+
+def test_lo_plane_carries_the_residual(pkg, orc):
+    # hi = 0, lo = arbitrary FP16: y = 2^-10 * (lo W^T), accumulated in FP32
+    g = torch.Generator().manual_seed(23)
+    M, N, K = 200, 320, 384
+    lo = (torch.randn((M, K), generator=g)).half()
+    W = (torch.randn((N, K), generator=g) * 0.05).half()
+    hi = torch.zeros_like(lo)
+    y = pkg.comp_gemm_f16x2(hi.cuda(), lo.cuda(), W.cuda()).cpu().double()
+    exact = (lo.double() @ W.double().t()) * 2.0**-10
+    den = (lo.double().abs() @ W.double().abs().t()) * 2.0**-10
+    assert torch.all((y - exact).abs() <= 4e-6 * den + 1e-30)
+
+
+def test_one_hot_and_identity(pkg):
+    K, N = 192, 320
+    W = (torch.randn(N, K) * 0.02).half()
+    x = torch.eye(K, dtype=torch.float32)
+    y = pkg.comp_gemm_f32x16_ws(x.cuda(), W.cuda()).cpu()
+    assert torch.equal(y, W.float().t())
+    x = torch.randn(200, 256) * 50
+    y = pkg.comp_gemm_f32x16_ws(x.cuda(), torch.eye(256, dtype=torch.float16).cuda()).cpu().double()
+    assert torch.all((y - x.double()).abs() <= 2.0**-22 * x.double().abs() + 2.0**-35)
+
+
+def test_small_workspace_falls_back_bitwise(pkg):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = 130, 300, 72
+    x, W = workloads.random_case(M, N, K, seed=31)
+    x, W = x.cuda(), W.cuda()
+    need = pkg.comp_gemm_workspace_bytes(M, K)
+    assert need == 4 * M * K
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    y_small = pkg.comp_gemm_f32x16_ws(x, W, workspace=ws)
+    y_fused = pkg.comp_gemm_f32x16(x, W)
+    assert torch.equal(bits(y_small), bits(y_fused))
+
+
+def test_deterministic_and_workspace_reuse(pkg):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs("encoder")
+    x, W = x.cuda(), W.cuda()
+    ws = torch.full((pkg.comp_gemm_workspace_bytes(*x.shape),), 0xFF, dtype=torch.uint8, device="cuda")
+    y1 = pkg.comp_gemm_f32x16_ws(x, W, workspace=ws)
+    y2 = pkg.comp_gemm_f32x16_ws(x, W, workspace=ws)
+    assert torch.equal(bits(y1), bits(y2))
+
+
+def test_output_guard_bands(pkg, orc):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = 130, 300, 72
+    x, W = workloads.random_case(M, N, K, seed=77)
+    pad = 4096
+    buf = torch.full((M * N + 2 * pad,), float("nan"), device="cuda")
+    y = buf[pad:pad + M * N].view(M, N)
+    wsbuf = torch.full((4 * M * K + 2 * pad,), 0xAB, dtype=torch.uint8, device="cuda")
+    ws = wsbuf[pad:pad + 4 * M * K]
+    pkg.comp_gemm_f32x16_ws(x.cuda(), W.cuda(), y, workspace=ws)
+    check_comp(y, x, W, orc)
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + M * N:]).all()
+    assert (wsbuf[:pad] == 0xAB).all() and (wsbuf[pad + 4 * M * K:] == 0xAB).all()
+
+
+def test_invalid_arguments(pkg):
+    from compensated_fp32_projection_gb300 import CompError
+
+    M, N, K = 64, 64, 64
+    x = torch.randn(M, K, device="cuda")
+    W = torch.randn(N, K, device="cuda").half()
+    # workspace overlapping x
+    with pytest.raises(CompError):
+        pkg.comp_gemm_f32x16_ws(x, W, workspace=x.view(torch.uint8))
+    # misaligned planes for the direct call
+    planes = torch.zeros(2 * M * K + 8, dtype=torch.float16, device="cuda")
+    hi = planes[1:1 + M * K].view(M, K)
+    lo = planes[1 + M * K:1 + 2 * M * K].view(M, K)
+    with pytest.raises(CompError):
+        pkg.comp_gemm_f16x2(hi, lo, W)
+    # K not a multiple of 8 for the direct call
+    h7 = torch.zeros(M, 7, dtype=torch.float16, device="cuda")
+    with pytest.raises(CompError):
+        pkg.comp_gemm_f16x2(h7, h7.clone(), torch.zeros(N, 7, dtype=torch.float16, device="cuda"))
+
+
+def test_k_zero_and_empty(pkg):
+    x = torch.empty(4, 0, device="cuda")
+    W = torch.empty(6, 0, dtype=torch.float16, device="cuda")
+    y = torch.full((4, 6), 7.0, device="cuda")
+    pkg.comp_gemm_f32x16_ws(x, W, y)
+    assert torch.equal(y.cpu(), torch.zeros(4, 6))
+    h = torch.empty(4, 0, dtype=torch.float16, device="cuda")
+    y.fill_(7.0)
+    pkg.comp_gemm_f16x2(h, h, W, y)
+    assert torch.equal(y.cpu(), torch.zeros(4, 6))
+
+
+def test_device_status_clean(pkg):
+    st, where = pkg.device_status()
+    assert st == 0 and where == 0
