@@ -1,10 +1,12 @@
 """Benchmark of the compensated-FP32 projection on GB300.
 
 One step is one compensated projection y = x W^T of the 4096 x 4096 x 4096
-square shape (x FP32 ~ N(0,1), W FP16 ~ N(0,0.02)) through the fused kernel
-comp_gemm_f32x16, which performs the whole path: the split of x into FP16
-hi/lo, both tensor-core products and the FP32 merge.  The metric is effective
-FP32-GEMM throughput, 2*M*N*K per second.
+square shape (x FP32 ~ N(0,1), W FP16 ~ N(0,0.02)) through the two-pass form
+of the path, the two launches comp_gemm_f32x16_ws makes: comp_split_f32 writes
+the FP16 hi/lo planes of x into a preallocated workspace, then comp_gemm_f16x2
+runs both tensor-core products and the FP32 merge.  The metric is effective
+FP32-GEMM throughput, 2*M*N*K per second.  The fused single-kernel
+comp_gemm_f32x16 is timed beside it and reported under "kernels".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -38,7 +40,7 @@ METRIC = "comp-FP32 GEMM effective TFLOPS (2MNK/s) & % of FP16 TC roofline; spli
 UNIT = "TFLOP/s"
 WORKLOAD = "square"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "comp_gemm_f32x16_square.md")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "comp_gemm_f16x2_square.md")
 KERNEL_SOURCE = os.path.join(ROOT, "compensated_fp32_projection_gb300", "csrc", "gemm_tc.cu")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -280,11 +282,21 @@ def run_ours(args):
     x = x_cpu.to(dev)
     W = W_cpu.to(dev)
     y = torch.empty((s.M, s.N), dtype=torch.float32, device=dev)
+    ws = torch.empty(pkg.comp_gemm_workspace_bytes(s.M, s.K), dtype=torch.uint8, device=dev)
+    hi = ws[: 2 * s.M * s.K].view(torch.float16).view(s.M, s.K)
+    lo = ws[2 * s.M * s.K:].view(torch.float16).view(s.M, s.K)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def split():
+        pkg.comp_split_f32(x, hi, lo)
+
+    def product():
+        pkg.comp_gemm_f16x2(hi, lo, W, y)
+
     def step():
-        pkg.comp_gemm_f32x16(x, W, y)
+        split()
+        product()
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -305,14 +317,19 @@ def run_ours(args):
     for _ in range(args.steps):
         flush.zero_()
         a = torch.cuda.Event(enable_timing=True)
+        m = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        step()
+        split()
+        m.record(stream)
+        product()
         b.record(stream)
-        events.append((a, b))
+        events.append((a, m, b))
     barrier()
     clocks = sampler.stop()
-    times = [a.elapsed_time(b) for a, b in events]  # ms
+    times = [a.elapsed_time(b) for a, _, b in events]  # ms, whole step
+    split_times = [a.elapsed_time(m) for a, m, _ in events]
+    product_times = [m.elapsed_time(b) for _, m, b in events]
     ms = statistics.mean(times)
     if dist is not None:
         t = torch.tensor([ms], device=dev)
@@ -333,7 +350,7 @@ def run_ours(args):
     for _ in range(2):
         x.copy_(x_h, non_blocking=True)
         W.copy_(W_h, non_blocking=True)
-        pkg.comp_gemm_f32x16(x, W, y)
+        pkg.comp_gemm_f32x16_ws(x, W, y, workspace=ws)
         y_h.copy_(y, non_blocking=True)
     barrier()
     a = torch.cuda.Event(enable_timing=True)
@@ -342,7 +359,7 @@ def run_ours(args):
     for _ in range(e2e_steps):
         x.copy_(x_h, non_blocking=True)
         W.copy_(W_h, non_blocking=True)
-        pkg.comp_gemm_f32x16(x, W, y)
+        pkg.comp_gemm_f32x16_ws(x, W, y, workspace=ws)
         y_h.copy_(y, non_blocking=True)
     b.record(stream)
     barrier()
@@ -354,8 +371,9 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     tensor_flops = 2.0 * flops  # two FP16 products per effective FP32 multiply-add
-    achieved = tensor_flops / (statistics.mean(times) * 1e-3) / 1e12
+    achieved = tensor_flops / (statistics.mean(product_times) * 1e-3) / 1e12
     traffic = measured_traffic()
+    split_in_step_gbs = 8.0 * s.M * s.K / (statistics.mean(split_times) * 1e-3) / 1e9
 
     # the standalone split and merge at the square shape's size (HBM bound), and the SIMT reference
     n = s.M * s.K
@@ -369,6 +387,8 @@ def run_ours(args):
     o32 = torch.empty(n, device=dev)
     med, mean = time_kernel(lambda: pkg.comp_merge_f32(a32, b32, o32), flush, stream, 20)
     merge_gbs = 12.0 * n / (mean * 1e-3) / 1e9
+    med, mean = time_kernel(lambda: pkg.comp_gemm_f32x16(x, W, y), flush, stream, 50)
+    fused_tflops = flops / (mean * 1e-3) / 1e12
     med, mean = time_kernel(lambda: pkg.comp_gemm_f32_simt(x, W, y), flush, stream, 3, warm=1)
     simt_tflops = flops / (mean * 1e-3) / 1e12
     del xs, hi, lo, a32, b32, o32
@@ -398,7 +418,8 @@ def run_ours(args):
         "data": "synthetic",
         "config": {
             "workload": f"{WORKLOAD} dense projection {s.M}x{s.N}x{s.K}: x FP32 N(0,1), W FP16 N(0,0.02) RNE, "
-                        f"y FP32; fused comp_gemm_f32x16 (split, two FP16 tensor-core products, FP32 merge)",
+                        f"y FP32; two-pass: comp_split_f32 into a workspace, then comp_gemm_f16x2 (two FP16 "
+                        f"tensor-core products, FP32 merge) - the launches of comp_gemm_f32x16_ws",
             "M": s.M,
             "N": s.N,
             "K": s.K,
@@ -408,6 +429,7 @@ def run_ours(args):
         },
         "roofline": {
             "bound": "tensor",
+            "kernel": "comp_f16x2_kernel (comp_gemm_f16x2)",
             "achieved": achieved,
             "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s",
@@ -415,7 +437,7 @@ def run_ours(args):
             "traffic": traffic,
             "peak_source": f"{peak_src} dense bf16 burst (FP16 runs at the same tensor rate)",
             "work": "4*M*N*K tensor FLOP per launch (hi and lo products)",
-            "effective_frac_of_roofline": value / world / (peaks["bf16_tflops"] / 2.0),
+            "step_frac_of_roofline": value / world / (peaks["bf16_tflops"] / 2.0),
         },
         "e2e": {
             "value": world * flops / (e2e_ms * 1e-3) / 1e12,
@@ -423,8 +445,13 @@ def run_ours(args):
             "h2d_bytes_per_step": 4 * s.M * s.K + 2 * s.N * s.K,
             "d2h_bytes_per_step": 4 * s.M * s.N,
         },
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,
         "kernels": {
+            "comp_split_f32 in step": {"n": s.M * s.K, "GB/s": split_in_step_gbs,
+                                       "frac_of_hbm": split_in_step_gbs / peaks["hbm_gbs"]},
+            "comp_gemm_f16x2 in step": {"ms": statistics.mean(product_times), "tensor TFLOP/s": achieved},
+            "comp_gemm_f32x16 (fused)": {"TFLOP/s": fused_tflops,
+                                         "frac_of_roofline": fused_tflops / (peaks["bf16_tflops"] / 2.0)},
             "comp_split_f32": {"n": n, "GB/s": split_gbs, "frac_of_hbm": split_gbs / peaks["hbm_gbs"]},
             "comp_merge_f32": {"n": n, "GB/s": merge_gbs, "frac_of_hbm": merge_gbs / peaks["hbm_gbs"]},
             "comp_gemm_f32_simt": {"TFLOP/s": simt_tflops},
