@@ -25,6 +25,7 @@ __all__ = [
     "comp_gemm_f16x2",
     "comp_gemm_f32x16_ws",
     "comp_gemm_workspace_bytes",
+    "comp_gemm_f32x16_noalloc",
     "device_status",
     "status_string",
 ]
@@ -160,4 +161,14 @@ def comp_gemm_f32x16_ws(x, W, y=None, workspace=None, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _native.call("comp_gemm_f32x16_ws", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K, workspace.data_ptr(),
                  nbytes, _stream(x, stream))
+    return y
+
+
+def comp_gemm_f32x16_noalloc(x, W, y=None, stream=None):
+    """comp_gemm_f32x16_ws with the library's static 64 MiB device workspace,
+    for callers that cannot allocate device memory per call (4*M*K must fit).
+    Calls on unordered streams race on that shared workspace."""
+    M, N, K, y = _gemm_args(x, W, y)
+    _native.call("comp_gemm_f32x16_noalloc", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K,
+                 _stream(x, stream))
     return y

@@ -167,6 +167,33 @@ comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, i
                                   void* workspace, int64_t workspace_bytes, comp_stream_t stream);
 
 /*
+ * COMP_NOALLOC_MAX_WORKSPACE_BYTES — size of the static device workspace of
+ * comp_gemm_f32x16_noalloc: 64 MiB, i.e. 4 * M * K <= 67108864
+ * (M * K <= 16777216, e.g. a 4096 x 4096 activation).
+ */
+#define COMP_NOALLOC_MAX_WORKSPACE_BYTES (64LL * 1024 * 1024)
+
+/*
+ * comp_gemm_f32x16_noalloc — comp_gemm_f32x16_ws with the workspace taken from
+ * a static device array of COMP_NOALLOC_MAX_WORKSPACE_BYTES inside the library,
+ * so that the call allocates nothing.  The pages have no counterpart for this
+ * call: it exists for callers that cannot allocate device memory per call
+ * (a plain C host without a device allocator of its own; a latency-critical
+ * loop that cannot pay for cudaFree's device synchronisation).
+ *   Same arguments, layout, results and errors as comp_gemm_f32x16, plus
+ *   COMP_ERR_INVALID_VALUE when 4 * M * K exceeds
+ *   COMP_NOALLOC_MAX_WORKSPACE_BYTES (rejected, never truncated).
+ *   The first call on a device looks up the static array's device address
+ *   (cudaGetSymbolAddress, with that device current; COMP_ERR_CUDA if it
+ *   fails); make that first call before any stream capture.
+ *   The array is shared by all calls on the device: calls whose executions
+ *   overlap (unordered streams or threads) race on it.  Calls ordered on one
+ *   stream are safe.  Nothing in it needs to start at zero.
+ */
+comp_status_t comp_gemm_f32x16_noalloc(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N,
+                                       int64_t K, comp_stream_t stream);
+
+/*
  * comp_device_status — waits for `stream`, then reports and clears the fault
  * word that kernels of this library set when a bounded wait inside them gives
  * up (they then skip the rest of their work and exit cleanly, leaving the
