@@ -115,13 +115,20 @@ struct Barriers {
     int abort;
 };
 
+// Suspend-time hint (ns) of the polling waits; 0 polls with the plain
+// try_wait, whose own bounded wait window is the only pause.
+#ifndef COMP_WAIT_SUSPEND_NS
+#define COMP_WAIT_SUSPEND_NS 20000
+#endif
+
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int* abort_flag, uint32_t code)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const long long start = clock64();
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 20000))
+        if (COMP_WAIT_SUSPEND_NS > 0 ? mbar_try_wait_sleep(bar, parity, COMP_WAIT_SUSPEND_NS)
+                                     : mbar_try_wait(bar, parity))
             return true;
         if (*reinterpret_cast<volatile int*>(abort_flag))
             return false;
@@ -149,6 +156,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* a
 
 // Bounded wait for the copies or MMAs a role already issued before the CTA
 // exits after an abort; no fault code (the first failure has one).
+// Lane 0 waits and the warp takes its verdict; for consumers whose reads are
+// ordered by tcgen05.fence::after_thread_sync after this warp synchronisation
+// (tensor-memory loads), so the other lanes need not touch the barrier.
+__device__ __forceinline__ bool lane0_wait(uint64_t* bar, uint32_t parity, int* abort_flag, uint32_t code)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0)
+        ok = wait_bounded(bar, parity, abort_flag, code);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
 {
     const long long start = clock64();
@@ -270,17 +288,6 @@ __device__ __forceinline__ void umma_f16_ta_scale10(uint32_t d_tmem, uint32_t a_
         "setp.ne.b32 p, 1, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p, 10;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc)
-        : "memory");
-}
-
-// D = A * B^T + D * 2^-10 with A and B in shared memory.
-__device__ __forceinline__ void umma_f16_ss_scale10(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, 1, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p, 10;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc)
         : "memory");
 }
 
@@ -625,23 +632,26 @@ constexpr int kLaunchRegs = 168;
 constexpr int kCtrlRegs = 40;
 constexpr int kPromoRegs = 232;
 static_assert(128 * kCtrlRegs + 32 * kPromoters * kPromoRegs <= kThreads * kLaunchRegs, "register split");
-constexpr int kStages = 4;
 constexpr uint32_t kPlaneBytes = BM * BK * 2;  // 16 KB: a 128 x 64 FP16 box
 
-template <int BN>
+// BN: tile width; NS: pipeline stages; CH: K blocks per accumulation chunk
+// (tensor-core accumulation restarts every CH * 64 of K).
+template <int BN, int NS, int CH>
 struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+    static_assert(NS >= 2 && CH >= 1 && CH <= NS, "stages");
     static constexpr uint32_t kWBytes = BN * BK * 2;
     static constexpr uint32_t kStageBytes = 2 * kPlaneBytes + kWBytes;  // hi | lo | W
-    static constexpr size_t kSmem = 1024 + kStages * kStageBytes + 256;
+    static constexpr size_t kSmem = 1024 + NS * kStageBytes + 256;
     static_assert(kSmem <= 232448, "shared memory");
     static constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
     static constexpr int kHalf = BN / 2;
 };
 
+constexpr int kMaxStages = 8;
 struct Barriers {
-    uint64_t full[kStages];   // hi, lo and W boxes landed (TMA bytes)
-    uint64_t empty[kStages];  // MMAs reading the stage completed
+    uint64_t full[kMaxStages];   // hi, lo and W boxes landed (TMA bytes)
+    uint64_t empty[kMaxStages];  // MMAs reading the stage completed
     uint64_t dfull[2];        // accumulator buffer holds a finished chunk
     uint64_t dfree[2];        // promotion warps have read the accumulator buffer
     uint64_t drain;
@@ -656,13 +666,13 @@ constexpr uint32_t kFaultX2MmaFull = 0x502;
 constexpr uint32_t kFaultX2MmaFree = 0x503;
 constexpr uint32_t kFaultX2Promote = 0x504;
 
-template <int BN>
+template <int BN, int NS, int CH>
 __global__ void __launch_bounds__(x2::kThreads, 1)
     comp_f16x2_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
                       const __grid_constant__ CUtensorMap tmap_w, const Problem P)
 {
-    using C = x2::Cfg<BN>;
-    constexpr int NS = x2::kStages;
+    using C = x2::Cfg<BN, NS, CH>;
+    static_assert(NS <= x2::kMaxStages, "stages");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     x2::Barriers* bars = reinterpret_cast<x2::Barriers*>(smem + NS * C::kStageBytes);
@@ -722,20 +732,46 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
             if (*reinterpret_cast<volatile int*>(&bars->abort))
                 for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
                     drain_wait(&bars->full[g % NS], (g / NS) & 1);
-        } else if (warp == 1 && lane == 0) {
-            // ---------------- MMA issuer, one chunk (one or two K blocks) at a time ----------------
+        } else if (warp == 1) {
+            // ---------------- MMA issuer, one chunk of CH K blocks at a time ----------------
+            // The whole warp runs the loop, so descriptors are warp-uniform;
+            // lane 0 observes the barriers and issues the MMAs and commits.
+            const uint32_t leader = lane == 0 ? 1u : 0u;
             const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
-            bool ok = true;
+            // Everything chunk (g, c) of n blocks needs: the full barriers of its
+            // stages and, from the third chunk on, its accumulator buffer back from
+            // promotion.  The whole warp tests them with non-blocking phase tests
+            // (one broadcast access each, identical results in every lane).  The
+            // tests for the next chunk are issued before the current chunk's last
+            // block of MMAs and read after it, so that their shared-memory round
+            // trips overlap queued tensor work; only resources still pending are
+            // then waited for, after all of the current chunk is issued.
+            auto test_chunk = [&](int g, int c, int n) -> bool {
+                bool r = c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1);
+#pragma unroll
+                for (int i = 0; i < CH; ++i)
+                    if (i < n)
+                        r = mbar_test_wait(&bars->full[(g + i) % NS], ((g + i) / NS) & 1) && r;
+                return r;
+            };
+            auto wait_chunk = [&](int g, int c, int n) -> bool {
+                bool ok = true;
+                if (lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < CH; ++i)
+                        if (ok && i < n)
+                            ok = wait_bounded(&bars->full[(g + i) % NS], ((g + i) / NS) & 1, &bars->abort,
+                                              kFaultX2MmaFull);
+                    if (ok && c >= 2)
+                        ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort, kFaultX2MmaFree);
+                }
+                return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            };
             int g = 0, c = 0, kb = 0;
+            int n = (P.nk < CH) ? P.nk : CH;  // blocks in this chunk (chunks stay inside a tile)
+            bool ok = total == 0 || wait_chunk(0, 0, n);
             while (g < total && ok) {
-                const int n = (kb + 1 < P.nk) ? 2 : 1;  // blocks in this chunk (chunks stay inside a tile)
                 const int b = c & 1;
-                for (int i = 0; i < n && ok; ++i)
-                    ok = wait_bounded(&bars->full[(g + i) % NS], ((g + i) / NS) & 1, &bars->abort, kFaultX2MmaFull);
-                if (ok && c >= 2)
-                    ok = wait_bounded(&bars->dfree[b], ((c >> 1) - 1) & 1, &bars->abort, kFaultX2MmaFree);
-                if (!ok)
-                    break;
                 tc_fence_after();
                 const uint32_t d = tmem + b * BN;
                 // descriptor of stage s: hi at +0, lo at +16 KB, W at +32 KB (start field counts 16 bytes)
@@ -746,29 +782,39 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
                     const uint64_t a = sdesc(g + i, x2::kPlaneBytes), w = sdesc(g + i, 2 * x2::kPlaneBytes);
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j)
-                        umma_f16(d, a + 2 * j, w + 2 * j, C::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+                        umma_f16_by(leader, d, a + 2 * j, w + 2 * j, C::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
                 }
+                // the next chunk's coordinates
+                const int g2 = g + n, c2 = c + 1;
+                const int kb2 = (kb + n == P.nk) ? 0 : kb + n;
+                const int n2 = (P.nk - kb2 < CH) ? P.nk - kb2 : CH;
+                bool ready2 = true;
                 for (int i = 0; i < n; ++i) {  // hi * W^T; the first scales D by 2^-10 on input
                     const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * x2::kPlaneBytes);
+                    if (i == n - 1 && g2 < total)
+                        ready2 = test_chunk(g2, c2, n2);
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j) {
                         if (i == 0 && j == 0)
-                            umma_f16_ss_scale10(d, a, w, C::kIdesc);
+                            umma_f16_scale10_by(leader, d, a, w, C::kIdesc);
                         else
-                            umma_f16(d, a + 2 * j, w + 2 * j, C::kIdesc, 1u);
+                            umma_f16_by(leader, d, a + 2 * j, w + 2 * j, C::kIdesc, 1u);
                     }
-                    umma_commit(&bars->empty[(g + i) % NS]);
+                    umma_commit_by(leader, &bars->empty[(g + i) % NS]);
                 }
-                umma_commit(&bars->dfull[b]);
-                g += n;
-                ++c;
-                kb += n;
-                if (kb == P.nk)
-                    kb = 0;
+                umma_commit_by(leader, &bars->dfull[b]);
+                g = g2;
+                c = c2;
+                kb = kb2;
+                n = n2;
+                if (g < total && !ready2)
+                    ok = wait_chunk(g, c, n);
             }
             if (!ok) {
-                umma_commit(&bars->drain);
-                drain_wait(&bars->drain, 0);
+                umma_commit_by(leader, &bars->drain);
+                if (lane == 0)
+                    drain_wait(&bars->drain, 0);
+                __syncwarp();
             }
         }
     } else {
@@ -783,29 +829,31 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
         int g = 0, c = 0, kb = 0;
         int t = static_cast<int>(blockIdx.x);
         while (g < total) {
-            const int n = (kb + 1 < P.nk) ? 2 : 1;
+            const int n = (P.nk - kb < CH) ? P.nk - kb : CH;
             const int b = c & 1;
-            if (!warp_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultX2Promote))
+            // one warp polls the barrier; the others wait at a named barrier
+            // (no shared-memory traffic) and read the verdict from the abort flag
+            if (warp == 4)
+                (void)lane0_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultX2Promote);
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * x2::kPromoters) : "memory");
+            if (*reinterpret_cast<volatile int*>(&bars->abort))
                 break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * BN + wh * C::kHalf;
+            // all of this thread's columns in one round trip; the buffer goes back
+            // to the MMA warp before the additions
+            uint32_t v[C::kHalf];
 #pragma unroll
-            for (int c0 = 0; c0 < C::kHalf; c0 += 64) {  // up to 64 columns per round trip
-                uint32_t v[64];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (c0 + 16 * q < C::kHalf)
-                        tmem_ld16(taddr + c0 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 64; i += 2)
-                    if (c0 + i < C::kHalf)
-                        add2(R[c0 + i], R[c0 + i + 1], v[i], v[i + 1]);
-            }
+            for (int q = 0; q < C::kHalf / 16; ++q)
+                tmem_ld16(taddr + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars->dfree[b]);
+#pragma unroll
+            for (int i = 0; i < C::kHalf; i += 2)
+                add2(R[i], R[i + 1], v[i], v[i + 1]);
             g += n;
             ++c;
             kb += n;
@@ -984,10 +1032,11 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
 
 namespace {
 
-template <int BN>
+template <int BN, int NS, int CH>
 comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                            const DeviceInfo& dev, cudaStream_t stream)
 {
+    using C = x2::Cfg<BN, NS, CH>;
     static std::mutex mu;
     static bool done[64] = {};
     {
@@ -995,8 +1044,8 @@ comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const C
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (!done[dev.device]) {
-            if (cudaFuncSetAttribute(comp_f16x2_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(x2::Cfg<BN>::kSmem)) != cudaSuccess) {
+            if (cudaFuncSetAttribute(comp_f16x2_kernel<BN, NS, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(C::kSmem)) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return COMP_ERR_CUDA;
             }
@@ -1005,7 +1054,7 @@ comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const C
     }
     const int tiles = P.tiles_m * P.tiles_n;
     const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-    comp_f16x2_kernel<BN><<<grid, x2::kThreads, x2::Cfg<BN>::kSmem, stream>>>(th, tl, tw, P);
+    comp_f16x2_kernel<BN, NS, CH><<<grid, x2::kThreads, C::kSmem, stream>>>(th, tl, tw, P);
     return launch_status();
 }
 
@@ -1057,7 +1106,8 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
         !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, BM) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn)))
         return COMP_ERR_CUDA;
-    return bn == 192 ? launch_x2_bn<192>(th, tl, tw, P, dev, stream) : launch_x2_bn<128>(th, tl, tw, P, dev, stream);
+    return bn == 192 ? launch_x2_bn<192, 4, 2>(th, tl, tw, P, dev, stream)
+                     : launch_x2_bn<128, 4, 2>(th, tl, tw, P, dev, stream);
 }
 
 comp_status_t read_and_clear_fault(cudaStream_t stream, uint32_t* where)

@@ -52,6 +52,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of a phase: true if the phase with this parity has
+// completed, returning at once either way.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Like mbar_try_wait, but a thread whose phase is not complete sleeps in
 // hardware until the phase completes or about `hint_ns` nanoseconds pass,
 // instead of returning at once; a polling loop then costs no issue slots.
@@ -146,6 +161,57 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Warp-wide issue: the whole (converged) warp runs the issuing loop, so that
+// descriptors and addresses are warp-uniform values, and one elected lane
+// executes the tensor-core instruction (a predicate inside the same asm).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t elect_one_sync()
+{
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e;
+}
+
+__device__ __forceinline__ void umma_f16_by(uint32_t leader, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+
+// D = A*B + D * 2^-10 (scale-input-d), issued by the elected lane.
+__device__ __forceinline__ void umma_f16_scale10_by(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
+                                                    uint64_t b_desc, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, 1, 0;\n\t"
+        "setp.ne.b32 q, %4, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p, 10;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(leader)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_by(uint32_t leader, uint64_t* bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(leader)
+        : "memory");
 }
 
 // Warp-wide: 32 TMEM lanes x 32 consecutive 32-bit columns; thread i receives
