@@ -23,6 +23,7 @@ __all__ = [
     "comp_gemm_f32x16_variant",
     "comp_gemm_f32_simt",
     "comp_gemm_f16x2",
+    "comp_gemm_f16x2_variant",
     "comp_gemm_f32x16_ws",
     "comp_gemm_workspace_bytes",
     "comp_gemm_f32x16_noalloc",
@@ -124,6 +125,11 @@ def comp_gemm_f32_simt(x, W, y=None, stream=None):
 
 def comp_gemm_f16x2(hi, lo, W, y=None, stream=None):
     """y = hi W^T + 2^-10 lo W^T from the split planes of comp_split_f32 (FP32 out)."""
+    return comp_gemm_f16x2_variant(hi, lo, W, 0, y, stream)
+
+
+def comp_gemm_f16x2_variant(hi, lo, W, variant, y=None, stream=None):
+    """comp_gemm_f16x2 with a chosen kernel (0 auto, 1 one CTA per 128-row tile, 2 CTA pairs)."""
     torch = _torch()
     _check(hi, torch.float16, "hi")
     _check(lo, torch.float16, "lo")
@@ -138,8 +144,8 @@ def comp_gemm_f16x2(hi, lo, W, y=None, stream=None):
     _check(y, torch.float32, "y")
     if tuple(y.shape) != (M, N):
         raise ValueError("y must be [M, N]")
-    _native.call("comp_gemm_f16x2", hi.data_ptr(), lo.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K,
-                 _stream(hi, stream))
+    _native.call("comp_gemm_f16x2_variant", hi.data_ptr(), lo.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K,
+                 int(variant), _stream(hi, stream))
     return y
 
 

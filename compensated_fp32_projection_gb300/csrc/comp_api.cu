@@ -168,12 +168,14 @@ comp_status_t comp_gemm_f32_simt(const float* x, const uint16_t* W, float* y, in
     return launch_gemm_simt(x, W, y, M, N, K, dev, s);
 }
 
-comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
-                              int64_t N, int64_t K, comp_stream_t stream)
+comp_status_t comp_gemm_f16x2_variant(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
+                                      int64_t N, int64_t K, int variant, comp_stream_t stream)
 {
     DeviceInfo dev;
     bool empty;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (variant < 0 || variant > 2)
+        return COMP_ERR_INVALID_VALUE;
     const comp_status_t st = check_gemm(hi, 2, W, y, M, N, K, s, &dev, &empty);
     if (st != COMP_OK || empty)
         return st;
@@ -182,7 +184,13 @@ comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint
         return COMP_ERR_INVALID_VALUE;
     if (!gemm_f16x2_supported(hi, lo, W, K))
         return COMP_ERR_INVALID_VALUE;
-    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, dev, s);
+    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, variant, dev, s);
+}
+
+comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
+                              int64_t N, int64_t K, comp_stream_t stream)
+{
+    return comp_gemm_f16x2_variant(hi, lo, W, y, M, N, K, 0, stream);
 }
 
 int64_t comp_gemm_workspace_bytes(int64_t M, int64_t K)
@@ -218,7 +226,7 @@ comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, i
     const comp_status_t sp = launch_split(x, hi, lo, M * K, dev, s);
     if (sp != COMP_OK)
         return sp;
-    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, dev, s);
+    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, 0, dev, s);
 }
 
 comp_status_t comp_device_status(comp_stream_t stream, uint32_t* where)

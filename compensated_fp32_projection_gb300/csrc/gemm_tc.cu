@@ -298,6 +298,7 @@ struct Problem {
     int M, N, K;
     int tiles_m, tiles_n, nk;
     int vec_y;
+    int tma_y;  // y is written with tensor-map stores (kernels that support it)
 };
 
 // Tile t covers rows (t / tiles_n) * 128 .. and columns (t % tiles_n) * BN ..;
@@ -892,6 +893,348 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Two-pass product on CTA pairs.  A cluster of two CTAs computes a 256 x BN
+// tile with one tcgen05 instruction stream (.cta_group::2, M = 256) issued by
+// the leader CTA (rank 0): each CTA holds its own 128 rows of the hi and lo
+// planes and half of the tile's W rows (BN / 2) in shared memory, and its 128
+// rows x BN columns of the accumulator in tensor memory.  Each SM thus reads
+// half of W per MMA and loads half of W per stage, which keeps the tensor
+// core's operand reads plus the TMA writes within the SM's shared-memory
+// bandwidth.  The accumulation is that of comp_f16x2_kernel: per chunk of CH
+// K blocks, lo * W^T fresh, then hi * W^T with the chunk's first MMA scaling
+// the lo sums by 2^-10, promoted into FP32 registers in both CTAs.
+// Synchronisation: each CTA's producer waits on its own empty barriers (the
+// leader's commits multicast to both CTAs) and counts its TMA bytes on the
+// leader's full barrier; both CTAs' promotion warps hand the accumulator back
+// by arriving on the leader's dfree barrier.
+// ---------------------------------------------------------------------------
+namespace pair {
+constexpr int kPromoters = 8;
+constexpr int kThreads = 128 + 32 * kPromoters;  // warpgroup 0: producer, MMA issuer, two idle warps
+// 384 threads launch with 168 registers each (pool 64512): control 40,
+// promotion 232: 128*40 + 256*232 = 64512.  The build checks the 168.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 40;
+constexpr int kPromoRegs = 232;
+static_assert(128 * kCtrlRegs + 32 * kPromoters * kPromoRegs <= kThreads * kLaunchRegs, "register split");
+constexpr uint32_t kPlaneBytes = BM * BK * 2;  // one CTA's 128 rows x 64 of K, FP16
+constexpr int kMaxStages = 8;
+constexpr int kRows = 2 * BM;  // rows of a pair tile
+// y epilogue: each promotion warp stages 32 rows x 16 columns of FP32 (2 KB,
+// 64-byte swizzle) in one of two buffers and writes it with a TMA store.
+constexpr uint32_t kYPiece = 32 * 16 * 4;
+constexpr uint32_t kYStage = kPromoters * 2 * kYPiece;  // 32 KB
+constexpr uint32_t kBarBytes = 1024;
+
+// BN: the pair's tile width (each CTA holds BN / 2 rows of W); NS: stages;
+// CH: K blocks per accumulation chunk.
+template <int BN, int NS, int CH>
+struct Cfg {
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+    static_assert(NS >= 2 && NS <= kMaxStages && CH >= 1 && CH <= NS, "stages");
+    static_assert(2 * BN <= 512, "tensor memory: two accumulator buffers");
+    static constexpr uint32_t kWBytes = (BN / 2) * BK * 2;
+    static constexpr uint32_t kStageBytes = 2 * kPlaneBytes + kWBytes;  // hi | lo | W half
+    static_assert(kStageBytes % 1024 == 0, "stage alignment of the 128-byte swizzle");
+    static constexpr uint32_t kTxBytes = 2 * kStageBytes;  // both CTAs' loads count on the leader's barrier
+    static constexpr size_t kSmem = 1024 + NS * kStageBytes + kBarBytes + kYStage;
+    static_assert(kSmem <= 232448, "shared memory");
+    static constexpr uint32_t kIdesc = idesc_f16_f32(kRows, BN);
+    static constexpr int kHalf = BN / 2;  // columns per promotion thread
+    static_assert(kHalf % 16 == 0, "promotion loads 16 columns at a time");
+};
+
+struct Barriers {
+    uint64_t full[kMaxStages];   // leader: both CTAs' hi, lo and W boxes landed
+    uint64_t empty[kMaxStages];  // the stage's MMAs completed (commit multicast to both CTAs)
+    uint64_t dfull[2];           // accumulator buffer holds a finished chunk (multicast)
+    uint64_t dfree[2];           // leader: both CTAs' promotion warps have read the buffer
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+}  // namespace pair
+
+// Fault codes of the CTA-pair product kernel.
+constexpr uint32_t kFaultPairProducer = 0x701;
+constexpr uint32_t kFaultPairMma = 0x702;
+constexpr uint32_t kFaultPairPromote = 0x703;
+
+template <int BN, int NS, int CH>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
+    comp_f16x2_pair_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
+                           const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_y,
+                           const Problem P)
+{
+    using C = pair::Cfg<BN, NS, CH>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    pair::Barriers* bars = reinterpret_cast<pair::Barriers*>(smem + NS * C::kStageBytes);
+    static_assert(sizeof(pair::Barriers) <= pair::kBarBytes, "barrier area");
+    uint8_t* ystage = smem + NS * C::kStageBytes + pair::kBarBytes;  // 1024-aligned
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader_cta = rank == 0;
+    const int pair_id = static_cast<int>(blockIdx.x >> 1);
+    const int num_pairs = static_cast<int>(gridDim.x >> 1);
+    const int num_tiles = P.tiles_m * P.tiles_n;  // pair tiles of 256 x BN
+    const int my_tiles = pair_id < num_tiles ? (num_tiles - 1 - pair_id) / num_pairs + 1 : 0;
+    const int total = my_tiles * P.nk;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->dfull[b], 1);
+            mbar_init(&bars->dfree[b], 2 * pair::kPromoters);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmap_hi);
+        tma_prefetch_desc(&tmap_lo);
+        tma_prefetch_desc(&tmap_w);
+        if (P.tma_y)
+            tma_prefetch_desc(&tmap_y);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&bars->tmem_base, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised before any remote arrival
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(pair::kCtrlRegs));
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer (both CTAs): own rows of hi and lo, own half of W ----------------
+            const uint32_t full0 = mapa_shared(&bars->full[0], 0);  // the leader's full barriers
+            int issued = 0;
+            int t = pair_id, kb = 0;
+            for (int g = 0; g < total; ++g) {
+                const int s = g % NS;
+                if (g >= NS && !wait_bounded(&bars->empty[s], ((g / NS) - 1) & 1, &bars->abort, kFaultPairProducer))
+                    break;
+                const int m0 = tile_m(t, P) * pair::kRows + static_cast<int>(rank) * BM;
+                const int n0 = tile_n(t, P) * BN + static_cast<int>(rank) * (BN / 2);
+                const int k0 = kb * BK;
+                uint8_t* st = smem + s * C::kStageBytes;
+                const uint32_t fb = full0 + static_cast<uint32_t>(s) * 8u;
+                if (leader_cta)
+                    mbar_arrive_expect_tx(&bars->full[s], C::kTxBytes);
+                tma_load_2d_pair(st, &tmap_hi, fb, k0, m0);
+                tma_load_2d_pair(st + pair::kPlaneBytes, &tmap_lo, fb, k0, m0);
+                tma_load_2d_pair(st + 2 * pair::kPlaneBytes, &tmap_w, fb, k0, n0);
+                issued = g + 1;
+                if (++kb == P.nk) {
+                    kb = 0;
+                    t += num_pairs;
+                }
+            }
+            if (*reinterpret_cast<volatile int*>(&bars->abort)) {
+                if (leader_cta) {
+                    // the leader's full barriers count both CTAs' loads
+                    for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
+                        drain_wait(&bars->full[g % NS], (g / NS) & 1);
+                } else {
+                    // this CTA's loads complete on the leader's barriers: give them time to land
+                    const long long start = clock64();
+                    while (clock64() - start < (1ll << 22)) {
+                    }
+                }
+            }
+        } else if (warp == 1 && leader_cta) {
+            // ---------------- MMA issuer (leader CTA), one chunk of CH K blocks at a time ----------------
+            const uint32_t leader = lane == 0 ? 1u : 0u;
+            const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
+            auto test_chunk = [&](int g, int c, int n) -> bool {
+                bool r = c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1);
+#pragma unroll
+                for (int i = 0; i < CH; ++i)
+                    if (i < n)
+                        r = mbar_test_wait(&bars->full[(g + i) % NS], ((g + i) / NS) & 1) && r;
+                return r;
+            };
+            auto wait_chunk = [&](int g, int c, int n) -> bool {
+                bool ok = true;
+                if (lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < CH; ++i)
+                        if (ok && i < n)
+                            ok = wait_bounded(&bars->full[(g + i) % NS], ((g + i) / NS) & 1, &bars->abort,
+                                                      kFaultPairMma);
+                    if (ok && c >= 2)
+                        ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort,
+                                                  kFaultPairMma);
+                }
+                return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            };
+            int g = 0, c = 0, kb = 0;
+            int n = (P.nk < CH) ? P.nk : CH;
+            bool ok = total == 0 || wait_chunk(0, 0, n);
+            while (g < total && ok) {
+                const int b = c & 1;
+                tc_fence_after();
+                const uint32_t d = tmem + b * BN;
+                auto sdesc = [&](int blk, uint32_t off) {
+                    return desc0 + static_cast<uint64_t>(((blk % NS) * C::kStageBytes + off) >> 4);
+                };
+                for (int i = 0; i < n; ++i) {  // lo * W^T of the chunk; the very first overwrites D
+                    const uint64_t a = sdesc(g + i, pair::kPlaneBytes), w = sdesc(g + i, 2 * pair::kPlaneBytes);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)
+                        umma_f16_pair_by(leader, d, a + 2 * j, w + 2 * j, C::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+                }
+                const int g2 = g + n, c2 = c + 1;
+                const int kb2 = (kb + n == P.nk) ? 0 : kb + n;
+                const int n2 = (P.nk - kb2 < CH) ? P.nk - kb2 : CH;
+                bool ready2 = true;
+                for (int i = 0; i < n; ++i) {  // hi * W^T; the first scales D by 2^-10 on input
+                    const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * pair::kPlaneBytes);
+                    if (i == n - 1 && g2 < total)
+                        ready2 = test_chunk(g2, c2, n2);
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j) {
+                        if (i == 0 && j == 0)
+                            umma_f16_pair_scale10_by(leader, d, a, w, C::kIdesc);
+                        else
+                            umma_f16_pair_by(leader, d, a + 2 * j, w + 2 * j, C::kIdesc, 1u);
+                    }
+                    umma_commit_pair_by(leader, &bars->empty[(g + i) % NS], 0x3);
+                }
+                umma_commit_pair_by(leader, &bars->dfull[b], 0x3);
+                g = g2;
+                c = c2;
+                kb = kb2;
+                n = n2;
+                if (g < total && !ready2)
+                    ok = wait_chunk(g, c, n);
+            }
+            if (!ok) {
+                umma_commit_pair_by(leader, &bars->drain, 0x1);
+                if (lane == 0)
+                    drain_wait(&bars->drain, 0);
+                __syncwarp();
+            }
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(pair::kPromoRegs));
+        // ---------------- promotion (both CTAs): R += D per chunk, then store y ----------------
+        const int wq = warp & 3;         // TMEM lane quarter
+        const int wh = (warp - 4) >> 2;  // column half of the tile
+        const uint32_t dfree0 = mapa_shared(&bars->dfree[0], 0);  // the leader's dfree barriers
+        float R[C::kHalf];
+#pragma unroll
+        for (int i = 0; i < C::kHalf; ++i)
+            R[i] = 0.0f;
+        int g = 0, c = 0, kb = 0;
+        int t = pair_id;
+        uint8_t* ybuf = ystage + (warp - 4) * (2 * pair::kYPiece);
+        int ng = 0;  // y pieces stored by this warp (its bulk groups, alternating buffers)
+        while (g < total) {
+            const int n = (P.nk - kb < CH) ? P.nk - kb : CH;
+            const int b = c & 1;
+            // one warp polls the barrier; the others wait at a named barrier
+            if (warp == 4)
+                (void)lane0_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultPairPromote);
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * pair::kPromoters) : "memory");
+            if (*reinterpret_cast<volatile int*>(&bars->abort))
+                break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * BN + wh * C::kHalf;
+#pragma unroll
+            for (int c0 = 0; c0 < C::kHalf; c0 += 64) {  // up to 64 columns per round trip
+                uint32_t v[64];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (c0 + 16 * q < C::kHalf)
+                        tmem_ld16(taddr + c0 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 64; i += 2)
+                    if (c0 + i < C::kHalf)
+                        add2(R[c0 + i], R[c0 + i + 1], v[i], v[i + 1]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(dfree0 + static_cast<uint32_t>(b) * 8u);
+            g += n;
+            ++c;
+            kb += n;
+            if (kb == P.nk) {
+                // tile finished: R holds y[m, nb .. nb + BN/2) for this thread's row m
+                const int64_t row0 = static_cast<int64_t>(tile_m(t, P)) * pair::kRows + rank * BM + wq * 32;
+                const int64_t m = row0 + lane;
+                const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
+                if (P.tma_y) {
+                    // 16-column pieces through shared memory; the tensor-map store
+                    // clips rows >= M and columns >= N
+#pragma unroll
+                    for (int p = 0; p < C::kHalf / 16; ++p) {
+                        if (row0 >= P.M || nb + 16 * p >= P.N)
+                            continue;
+                        uint8_t* buf = ybuf + (ng & 1) * pair::kYPiece;
+                        if (ng >= 2) {  // the store that last read this buffer has finished reading it
+                            if (lane == 0)
+                                bulk_wait_group_read1();
+                            __syncwarp();
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)  // 64-byte swizzle: 16-byte chunk j of row `lane`
+                            st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), R[16 * p + 4 * j],
+                                         R[16 * p + 4 * j + 1], R[16 * p + 4 * j + 2], R[16 * p + 4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmap_y, buf, static_cast<int32_t>(nb + 16 * p), static_cast<int32_t>(row0));
+                            bulk_commit_group();
+                        }
+                        ++ng;
+                    }
+                } else if (m < P.M) {
+                    float* yrow = P.y + m * P.N;
+                    if (P.vec_y && nb + C::kHalf <= P.N) {
+#pragma unroll
+                        for (int i = 0; i < C::kHalf; i += 4)
+                            *reinterpret_cast<float4*>(yrow + nb + i) = make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < C::kHalf; ++i)
+                            if (nb + i < P.N)
+                                yrow[nb + i] = R[i];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < C::kHalf; ++i)
+                    R[i] = 0.0f;
+                kb = 0;
+                t += num_pairs;
+            }
+        }
+        if (lane == 0)
+            bulk_wait_group0();  // y stores complete
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still signal its barriers
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -918,7 +1261,8 @@ EncodeTiledFn encode_fn()
 // A 2-D row-major tensor (inner extent `inner` contiguous, `outer` rows) as a
 // tensor map with box_inner x box_outer boxes and the 128-byte swizzle.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, size_t elem, const void* base, int64_t inner,
-               int64_t outer, uint32_t box_inner, uint32_t box_outer)
+               int64_t outer, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -928,7 +1272,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, size_t elem, const v
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1013,6 +1357,7 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
     P.K = static_cast<int>(K);
     P.nk = static_cast<int>((K + BK - 1) / BK);
     P.vec_y = (N % 4 == 0) && aligned16(y);
+    P.tma_y = 0;
     const int bn = pick_bn(M, N, dev.sm_count);
     P.tiles_m = static_cast<int>((M + BM - 1) / BM);
     P.tiles_n = static_cast<int>((N + bn - 1) / bn);
@@ -1058,6 +1403,44 @@ comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const C
     return launch_status();
 }
 
+template <int BN, int NS, int CH>
+comp_status_t launch_pair_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const CUtensorMap& ty,
+                             const Problem& P, const DeviceInfo& dev, cudaStream_t stream)
+{
+    using C = pair::Cfg<BN, NS, CH>;
+    static std::mutex mu;
+    static int pairs[64] = {};  // co-resident CTA pairs per device, 0 = not yet known
+    int np;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev.device < 0 || dev.device >= 64)
+            return COMP_ERR_CUDA;
+        if (pairs[dev.device] == 0) {
+            if (cudaFuncSetAttribute(comp_f16x2_pair_kernel<BN, NS, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(C::kSmem)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return COMP_ERR_CUDA;
+            }
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count & ~1), 1, 1);
+            cfg.blockDim = dim3(pair::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = C::kSmem;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, comp_f16x2_pair_kernel<BN, NS, CH>, &cfg) != cudaSuccess ||
+                clusters <= 0) {
+                (void)cudaGetLastError();
+                clusters = dev.sm_count / 2;
+            }
+            pairs[dev.device] = clusters;
+        }
+        np = pairs[dev.device];
+    }
+    const int tiles = P.tiles_m * P.tiles_n;
+    const int grid = 2 * (tiles < np ? tiles : np);
+    comp_f16x2_pair_kernel<BN, NS, CH><<<grid, pair::kThreads, C::kSmem, stream>>>(th, tl, tw, ty, P);
+    return launch_status();
+}
+
 // N tile width for the two-pass product (tiles are all tensor work there).
 int pick_bn_x2(int64_t M, int64_t N, int sms)
 {
@@ -1075,6 +1458,24 @@ int pick_bn_x2(int64_t M, int64_t N, int sms)
     return best;
 }
 
+// Pair-tile width for the CTA-pair product: fewest rounds of pair tiles over
+// the co-resident pairs, weighted by the tile width.
+int pick_bn_pair(int64_t M, int64_t N, int pairs)
+{
+    static const int cands[] = {224, 256};
+    int best = 256;
+    int64_t best_cost = INT64_MAX;
+    for (int bn : cands) {
+        const int64_t tiles = ((M + pair::kRows - 1) / pair::kRows) * ((N + bn - 1) / bn);
+        const int64_t cost = ((tiles + pairs - 1) / pairs) * (bn + 32);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
 }  // namespace
 
 bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t K)
@@ -1083,10 +1484,13 @@ bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t
 }
 
 comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
-                                int64_t N, int64_t K, const DeviceInfo& dev, cudaStream_t stream)
+                                int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream)
 {
-    if (!gemm_f16x2_supported(hi, lo, W, K))
+    if (!gemm_f16x2_supported(hi, lo, W, K) || variant < 0 || variant > 2)
         return COMP_ERR_INVALID_VALUE;
+    // CTA pairs once the output fills about one wave of single-CTA tiles: below
+    // that, pipeline fill dominates and the 128-row tiles spread over more SMs.
+    const bool pairs = variant == 2 || (variant == 0 && M > BM && M * N >= static_cast<int64_t>(dev.sm_count) * BM * 192);
     Problem P;
     P.x = nullptr;
     P.W = W;
@@ -1096,12 +1500,32 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     P.K = static_cast<int>(K);
     P.nk = static_cast<int>((K + BK - 1) / BK);
     P.vec_y = (N % 4 == 0) && aligned16(y);
+    P.tma_y = 0;
+    CUtensorMap th{}, tl{}, tw{};
+    if (pairs) {
+        // CTA pairs on 256-row tiles
+        const int bn = pick_bn_pair(M, N, dev.sm_count / 2);
+        P.tiles_m = static_cast<int>((M + pair::kRows - 1) / pair::kRows);
+        P.tiles_n = static_cast<int>((N + bn - 1) / bn);
+        if (static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
+            return COMP_ERR_INVALID_VALUE;
+        CUtensorMap ty{};
+        if (!encode_2d(&th, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hi, K, M, BK, BM) ||
+            !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, BM) ||
+            !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn / 2)))
+            return COMP_ERR_CUDA;
+        if (P.vec_y)
+            P.tma_y = encode_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, N, M, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B)
+                          ? 1
+                          : 0;
+        return bn == 224 ? launch_pair_bn<224, 4, 2>(th, tl, tw, ty, P, dev, stream)
+                         : launch_pair_bn<256, 4, 2>(th, tl, tw, ty, P, dev, stream);
+    }
     const int bn = pick_bn_x2(M, N, dev.sm_count);
     P.tiles_m = static_cast<int>((M + BM - 1) / BM);
     P.tiles_n = static_cast<int>((N + bn - 1) / bn);
     if (static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
         return COMP_ERR_INVALID_VALUE;
-    CUtensorMap th{}, tl{}, tw{};
     if (!encode_2d(&th, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hi, K, M, BK, BM) ||
         !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, BM) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn)))

@@ -219,3 +219,39 @@ def test_k_zero_and_empty(pkg):
 def test_device_status_clean(pkg):
     st, where = pkg.device_status()
     assert st == 0 and where == 0
+
+
+# both product kernels on every tile shape: one CTA per 128-row tile (1) and
+# CTA pairs per 256-row tile (2)
+@pytest.mark.parametrize("shape", SHAPES + [(2048, 2048, 256), (2000, 2001, 136), (300, 4096, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("variant", [1, 2])
+def test_product_kernels(pkg, orc, shape, variant):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=M * 7 + N * 3 + K, scale=2.0)
+    hi, lo = pkg.comp_split_f32(x.cuda())
+    y = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), variant)
+    check_comp(y, x, W, orc)
+
+
+def test_product_kernels_agree(pkg, orc):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.random_case(1024, 1536, 512, seed=5)
+    hi, lo = pkg.comp_split_f32(x.cuda())
+    y1 = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), 1)
+    y2 = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), 2)
+    e1, _ = check_comp(y1, x, W, orc)
+    e2, _ = check_comp(y2, x, W, orc)
+    den = (x.double().abs() @ W.double().abs().t()).cuda()
+    assert torch.all((y1.double() - y2.double()).abs() <= 2 * 4e-6 * den + 1e-30)
+
+
+def test_product_variant_out_of_range(pkg):
+    from compensated_fp32_projection_gb300 import CompError
+
+    h = torch.zeros(8, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(CompError):
+        pkg.comp_gemm_f16x2_variant(h, h.clone(), torch.zeros(16, 64, dtype=torch.float16, device="cuda"), 3)
