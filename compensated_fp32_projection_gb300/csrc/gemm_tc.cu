@@ -4,11 +4,10 @@
 //   - compensated-FP32 paragraph: each FP32 input is split into two FP16
 //     components, both products with the exact FP16 weights accumulate in FP32,
 //     and the two are combined in FP32;
-//   - "The fused split/merge build" paragraph: split and merge fused into the
-//     projection;
-//   - AMD paragraph: accumulating tile results with separate FP32 additions,
-//     rather than one long chain of cooperative-matrix multiply-adds, removes the
-//     accumulation drift of long dot products.
+//   - fused-build paragraph: split and merge folded into the projection;
+//   - AMD paragraph: partial results of the tiles are summed by plain FP32
+//     additions instead of one long chain of cooperative-matrix multiply-adds,
+//     which removes the accumulation drift of long dot products.
 //
 // A persistent CTA computes 128 x BN tiles of y.  Per tile and K block of 64:
 //   1. TMA brings the 128 x 64 FP32 block of x (two 128x32 boxes, 128-byte
@@ -1444,10 +1443,26 @@ comp_status_t launch_pair_bn(const CUtensorMap& th, const CUtensorMap& tl, const
 // N tile width for the two-pass product (tiles are all tensor work there).
 int pick_bn_x2(int64_t M, int64_t N, int sms)
 {
-    static const int cands[] = {192, 128};
+    static const int cands[] = {192, 128, 96};
+    if (M <= BM) {
+        // one row of tiles: the product streams W, so the tile width that keeps
+        // the most SMs busy per round wins (ties: the wider tile)
+        int best = 192;
+        double best_busy = -1.0;
+        for (int bn : cands) {
+            const int64_t tiles = (N + bn - 1) / bn;
+            const int64_t rounds = (tiles + sms - 1) / sms;
+            const double busy = static_cast<double>(tiles) / static_cast<double>(rounds);
+            if (busy > best_busy + 0.5) {
+                best_busy = busy;
+                best = bn;
+            }
+        }
+        return best;
+    }
     int best = 128;
     int64_t best_cost = INT64_MAX;
-    for (int bn : cands) {
+    for (int bn : {192, 128}) {  // narrower MMAs would be issue-bound
         const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
         const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 32);
         if (cost < best_cost) {
@@ -1530,8 +1545,11 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
         !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, BM) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn)))
         return COMP_ERR_CUDA;
-    return bn == 192 ? launch_x2_bn<192, 4, 2>(th, tl, tw, P, dev, stream)
-                     : launch_x2_bn<128, 4, 2>(th, tl, tw, P, dev, stream);
+    if (bn == 192)
+        return launch_x2_bn<192, 4, 2>(th, tl, tw, P, dev, stream);
+    if (bn == 128)
+        return launch_x2_bn<128, 4, 2>(th, tl, tw, P, dev, stream);
+    return launch_x2_bn<96, 4, 2>(th, tl, tw, P, dev, stream);
 }
 
 comp_status_t read_and_clear_fault(cudaStream_t stream, uint32_t* where)

@@ -1,5 +1,6 @@
-// The standalone split and merge kernels (laya.cpp docs/vulkan.md: "Each input
-// split and output merge uses a single GPU dispatch").  Both are streaming,
+// The standalone split and merge kernels (laya.cpp docs/vulkan.md, split/merge
+// paragraph: the split of an input and the merge of an output are one dispatch
+// each).  Both are streaming,
 // HBM-bound kernels: 128-bit coalesced loads, 64/128-bit coalesced stores,
 // evict-first cache hints, grid-stride loops over a grid sized to the SM count.
 //

@@ -3,18 +3,15 @@
  *
  * The method is the "compensated FP32" projection of laya.cpp's Vulkan backend
  * page (docs/vulkan.md):
- *   - paragraph "Compensated FP32 splits each projection input into two FP16
- *     components ...": every FP32 activation x is split into two FP16 values,
- *     both are multiplied by the FP16 weights (which are stored exactly) with
- *     FP32 accumulators, and the two results are combined in FP32;
- *   - paragraph "Each input split and output merge uses a single GPU dispatch":
- *     the split rounds to nearest-even, including subnormals, and scales the
- *     residual by 1024;
- *   - paragraph "A build-time extension of the pinned Vulkan backend supplies
- *     true FP32 matrix kernels": a plain FP32 matrix product that never converts
- *     its FP32 operand to FP16;
- *   - paragraph "The fused split/merge build": split and merge fused into the
- *     projection.
+ *   - compensated-FP32 paragraph: every FP32 activation x becomes two FP16
+ *     values, both multiplied by the exactly stored FP16 weights with FP32
+ *     accumulators, and the two results are combined in FP32;
+ *   - split/merge paragraph: the split rounds to nearest with ties to even,
+ *     keeps subnormal results, and multiplies the residual by 1024; each split
+ *     and each merge is one dispatch;
+ *   - true-FP32 kernels paragraph: an optional build with plain FP32 matrix
+ *     kernels that never convert the FP32 operand to FP16;
+ *   - fused-build paragraph: split and merge folded into the projection.
  * In formulas, with fp16_rne the IEEE 754 binary32 -> binary16 conversion
  * (round to nearest, ties to even, gradual underflow, overflow to infinity):
  *     hi = fp16_rne(x)                 lo = fp16_rne((x - hi) * 1024)
@@ -39,8 +36,8 @@
  *   - Argument errors are detected before anything is enqueued and return
  *     COMP_ERR_INVALID_VALUE.  A device that is not compute capability 10.3
  *     returns COMP_ERR_UNSUPPORTED_DEVICE.  There is no CPU fallback (as on the
- *     laya.cpp page: "An unavailable backend produces an error; there is no
- *     automatic CPU fallback").
+ *     laya.cpp page's backend-selection paragraph, where a missing backend is
+ *     an error and nothing falls back to the CPU).
  *   - Sizes of zero are valid no-ops, except that a GEMM with K == 0 and
  *     M*N > 0 writes y = +0.
  */
@@ -92,7 +89,7 @@ comp_status_t comp_merge_f32(const float* acc_hi, const float* acc_lo, float* y,
 
 /*
  * comp_gemm_f32x16 — the fused compensated projection (laya.cpp docs/vulkan.md,
- * compensated-FP32 paragraph and "The fused split/merge build" paragraph):
+ * compensated-FP32 paragraph and the fused-build paragraph):
  *   y[m,n] = acc_hi[m,n] + acc_lo[m,n] * 2^-10, with acc_hi, acc_lo the FP32
  *   tensor-core accumulations of hi(x)·W^T and lo(x)·W^T.
  *   x : [M, K] binary32 (input).   W : [N, K] binary16 (input).   y : [M, N] binary32 (output).

@@ -7,15 +7,15 @@
  * includes nothing from it.
  *
  * Source of the method: laya.cpp, "docs/vulkan.md" (Vulkan backend page),
- *   - paragraph "Compensated FP32 splits each projection input into two FP16
- *     components ..." : two FP16 components per input, both products with FP32
- *     accumulators, combined in FP32; FP16 weights are exact;
- *   - paragraph "Each input split and output merge uses a single GPU dispatch ..." :
- *     round to nearest-even including subnormals, residual scaled by 1024;
- *   - paragraph on the compensated acceptance ("The residual component uses a
- *     scale of 1024 to avoid FP16 overflow at large activations").
- * The merge formula y = acc_hi + acc_lo * 2^-10 is the plain reading of
- * "combines them in FP32" with the 1024 scale undone.
+ *   - compensated-FP32 paragraph: each FP32 input becomes two FP16 components,
+ *     each multiplied by the exactly stored FP16 weights with FP32 accumulation,
+ *     and the two results are combined in FP32;
+ *   - split/merge paragraph: the split rounds to nearest, ties to even, keeping
+ *     subnormal results, and the residual is multiplied by 1024;
+ *   - 1024-scale paragraph: why the residual is scaled by 2^10 (so that it
+ *     cannot overflow binary16 for large activations).
+ * The merge formula y = acc_hi + acc_lo * 2^-10 is the plain reading of the
+ * FP32 combination with the 1024 scale undone.
  *
  * Every floating-point step here is done in IEEE double, where each step used is
  * exact, and then rounded once to the target format.  Compile with

@@ -1,6 +1,6 @@
 """GPU parity of the standalone split and merge kernels: bit-exact against the
-CPU oracle (laya.cpp docs/vulkan.md, split/merge paragraph: "Operator tests
-check both packed components and the merged FP32 results bit-for-bit").
+CPU oracle (laya.cpp docs/vulkan.md, split/merge paragraph: the page's operator
+tests compare the two components and the merged FP32 values bit for bit).
 NaN outputs are compared by class (both NaN), not by payload."""
 import os
 

@@ -1,8 +1,8 @@
 """Pins for the oracle's binary16 rounding (fp16_rne), independent of the oracle.
 
 The rounding is the one the laya.cpp Vulkan page fixes for the split
-(docs/vulkan.md, split/merge paragraph: "rounds FP16 values to nearest-even,
-including subnormals").  It is checked here against
+(docs/vulkan.md, split/merge paragraph: round to nearest with ties to even, and
+subnormal binary16 results kept).  It is checked here against
 
 * brute force: the nearest of all 63,488 finite binary16 values (plus +-2^16
   standing in for +-inf), ties to the even fraction, found by exhaustive search;
