@@ -10,9 +10,12 @@ comp_gemm_f32x16 is timed beside it and reported under "kernels".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Timing: every step gets its own CUDA-event pair on the launching stream; the
-L2 cache (129 MB, larger than the 96 MB of inputs) is flushed by writing a
-256 MiB buffer before each step, outside the event pair.  The K timed steps
+Timing: every step gets its own CUDA-event pair on the launching stream.
+Before each step, outside the event pair, the L2 cache (129 MB, larger than
+the 96 MB of inputs) is flushed: a 256 MiB buffer is written, then another
+256 MiB buffer is read, so that the step starts with cold inputs and with L2
+holding clean lines (the write-back of the flush's own dirty lines is not
+charged to the step).  The K timed steps
 are bracketed by a barrier and a device synchronisation on both sides, and
 the slowest rank's time is reported.  N > 1 runs one independent replica per
 GPU (the path has no exchange step), so scaling is weak.
@@ -237,16 +240,35 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+class L2Flush:
+    """Cold, clean L2 before a timed launch: write a 256 MiB buffer (larger
+    than the 129 MB L2), then read a second one so that the written lines are
+    back in DRAM before the timed region starts."""
+
+    def __init__(self, dev):
+        import torch
+
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros((256 << 20) // 8, dtype=torch.int64, device=dev)
+        self.out = torch.empty((), dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        import torch
+
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.out)
+
+
 def time_kernel(fn, flush, stream, reps: int, warm: int = 3):
     """Median and mean of per-launch CUDA-event times (ms), L2 flushed before each."""
     import torch
 
     for _ in range(warm):
-        flush.zero_()
+        flush()
         fn()
     ts = []
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -285,7 +307,7 @@ def run_ours(args):
     ws = torch.empty(pkg.comp_gemm_workspace_bytes(s.M, s.K), dtype=torch.uint8, device=dev)
     hi = ws[: 2 * s.M * s.K].view(torch.float16).view(s.M, s.K)
     lo = ws[2 * s.M * s.K:].view(torch.float16).view(s.M, s.K)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     def split():
@@ -306,7 +328,7 @@ def run_ours(args):
 
     warm = max(3, args.warmup)
     for _ in range(warm):
-        flush.zero_()
+        flush()
         step()
     barrier()
     sampler = ClockSampler(dev.index)
@@ -315,7 +337,7 @@ def run_ours(args):
     barrier()
     events = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         m = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
@@ -424,7 +446,8 @@ def run_ours(args):
             "N": s.N,
             "K": s.K,
             "seed": workloads.SEED_BASE + s.index,
-            "l2": "flushed before every timed step (256 MiB write, outside the event pair)",
+            "l2": "flushed before every timed step, outside the event pair: 256 MiB written, then another "
+                  "256 MiB read (cold inputs, clean L2)",
             "replicas": world,
         },
         "roofline": {
