@@ -39,6 +39,7 @@
 #include <cuda_fp16.h>
 
 #include <mutex>
+#include <utility>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -715,6 +716,7 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
         if (warp == 0 && lane == 0) {
             // ---------------- TMA producer: hi, lo and W boxes per K block ----------------
             int issued = 0;
+            grid_dependency_wait();  // the planes come from the previous kernel of the stream
             Cursor<BN> cur;
             cur.start(P);
             for (int g = 0; g < total; ++g, cur.next(P)) {
@@ -1015,6 +1017,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(pair::kCtrlRegs));
         if (warp == 0 && lane == 0) {
             // ---------------- TMA producer (both CTAs): own rows of hi and lo, own half of W ----------------
+            grid_dependency_wait();  // the planes come from the previous kernel of the stream
             const uint32_t full0 = mapa_shared(&bars->full[0], 0);  // the leader's full barriers
             int issued = 0;
             int t = pair_id, kb = 0;
@@ -1376,6 +1379,30 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
 
 namespace {
 
+// Launch with programmatic stream serialisation: the kernel's set-up overlaps
+// the end of the previous kernel on the stream; its producer waits
+// (griddepcontrol.wait) before it reads what that kernel wrote.
+template <typename... KArgs, typename... Args>
+comp_status_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t smem, cudaStream_t stream,
+                         Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return COMP_ERR_LAUNCH;
+    }
+    return COMP_OK;
+}
+
 template <int BN, int NS, int CH>
 comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                            const DeviceInfo& dev, cudaStream_t stream)
@@ -1398,8 +1425,7 @@ comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const C
     }
     const int tiles = P.tiles_m * P.tiles_n;
     const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-    comp_f16x2_kernel<BN, NS, CH><<<grid, x2::kThreads, C::kSmem, stream>>>(th, tl, tw, P);
-    return launch_status();
+    return launch_pdl(comp_f16x2_kernel<BN, NS, CH>, grid, x2::kThreads, C::kSmem, stream, th, tl, tw, P);
 }
 
 template <int BN, int NS, int CH>
@@ -1436,8 +1462,7 @@ comp_status_t launch_pair_bn(const CUtensorMap& th, const CUtensorMap& tl, const
     }
     const int tiles = P.tiles_m * P.tiles_n;
     const int grid = 2 * (tiles < np ? tiles : np);
-    comp_f16x2_pair_kernel<BN, NS, CH><<<grid, pair::kThreads, C::kSmem, stream>>>(th, tl, tw, ty, P);
-    return launch_status();
+    return launch_pdl(comp_f16x2_pair_kernel<BN, NS, CH>, grid, pair::kThreads, C::kSmem, stream, th, tl, tw, ty, P);
 }
 
 // N tile width for the two-pass product (tiles are all tensor work there).

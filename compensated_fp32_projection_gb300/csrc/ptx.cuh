@@ -406,4 +406,22 @@ __device__ __forceinline__ void st_shared_v4(void* p, float a, float b, float c,
                  : "memory");
 }
 
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the previous kernel of the stream is still
+// running; griddepcontrol.wait blocks until that kernel has completed and its
+// memory is visible (a no-op for a normally launched kernel).
+// launch_dependents lets the next such kernel start early.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace compfp32

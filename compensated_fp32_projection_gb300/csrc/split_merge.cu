@@ -46,6 +46,9 @@ __device__ __forceinline__ void split4(const float4 v, uint2& hi, uint2& lo)
 __global__ void __launch_bounds__(kThreads) split_vec_kernel(const float4* __restrict__ x, uint2* __restrict__ hi,
                                                              uint2* __restrict__ lo, int64_t n4)
 {
+    // a product kernel launched after this one may start its set-up now; it
+    // waits for this grid's completion before it reads hi and lo
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     for (; i + (kUnroll - 1) * stride < n4; i += kUnroll * stride) {
