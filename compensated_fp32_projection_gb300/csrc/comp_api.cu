@@ -229,6 +229,15 @@ comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, i
     return launch_gemm_f16x2(hi, lo, W, y, M, N, K, 0, dev, s);
 }
 
+comp_status_t comp_check_wait_timeout(comp_stream_t stream)
+{
+    DeviceInfo dev;
+    const comp_status_t st = current_device(&dev);
+    if (st != COMP_OK)
+        return st;
+    return launch_check_wait_timeout(static_cast<cudaStream_t>(stream));
+}
+
 comp_status_t comp_device_status(comp_stream_t stream, uint32_t* where)
 {
     if (where)

@@ -633,23 +633,31 @@ constexpr int kLaunchRegs = 168;
 constexpr int kCtrlRegs = 40;
 constexpr int kPromoRegs = 232;
 static_assert(128 * kCtrlRegs + 32 * kPromoters * kPromoRegs <= kThreads * kLaunchRegs, "register split");
-constexpr uint32_t kPlaneBytes = BM * BK * 2;  // 16 KB: a 128 x 64 FP16 box
-
 // BN: tile width; NS: pipeline stages; CH: K blocks per accumulation chunk
-// (tensor-core accumulation restarts every CH * 64 of K).
-template <int BN, int NS, int CH>
+// (tensor-core accumulation restarts every CH * 64 of K); AR: rows of the hi
+// and lo boxes.  AR < 128 serves problems of at most AR rows: only AR rows of
+// each plane are loaded, so a stage is small and many stages stay in flight
+// while W streams.  The MMA still reads 128 rows from each plane's offset;
+// rows AR..127 read whatever follows inside the same stage, and since each
+// output row depends only on its own A row, those garbage rows only produce
+// outputs that are never stored.
+template <int BN, int NS, int CH, int AR = BM>
 struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
     static_assert(NS >= 2 && CH >= 1 && CH <= NS, "stages");
+    static_assert(AR == BM || AR == 32, "box rows");
+    static constexpr uint32_t kPlaneBytes = AR * BK * 2;  // an AR x 64 FP16 box
     static constexpr uint32_t kWBytes = BN * BK * 2;
     static constexpr uint32_t kStageBytes = 2 * kPlaneBytes + kWBytes;  // hi | lo | W
+    static_assert(kStageBytes % 1024 == 0, "stage alignment of the 128-byte swizzle");
+    static_assert(kPlaneBytes + BM * BK * 2 <= kStageBytes, "the 128-row read of the lo plane stays in its stage");
     static constexpr size_t kSmem = 1024 + NS * kStageBytes + 256;
     static_assert(kSmem <= 232448, "shared memory");
     static constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
     static constexpr int kHalf = BN / 2;
 };
 
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 struct Barriers {
     uint64_t full[kMaxStages];   // hi, lo and W boxes landed (TMA bytes)
     uint64_t empty[kMaxStages];  // MMAs reading the stage completed
@@ -667,16 +675,17 @@ constexpr uint32_t kFaultX2MmaFull = 0x502;
 constexpr uint32_t kFaultX2MmaFree = 0x503;
 constexpr uint32_t kFaultX2Promote = 0x504;
 
-template <int BN, int NS, int CH>
+template <int BN, int NS, int CH, int AR>
 __global__ void __launch_bounds__(x2::kThreads, 1)
     comp_f16x2_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
                       const __grid_constant__ CUtensorMap tmap_w, const Problem P)
 {
-    using C = x2::Cfg<BN, NS, CH>;
+    using C = x2::Cfg<BN, NS, CH, AR>;
     static_assert(NS <= x2::kMaxStages, "stages");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     x2::Barriers* bars = reinterpret_cast<x2::Barriers*>(smem + NS * C::kStageBytes);
+    static_assert(sizeof(x2::Barriers) <= 256, "barrier area");
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -727,8 +736,8 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
                 const int k0 = cur.kb * BK;
                 mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
                 tma_load_2d(st, &tmap_hi, &bars->full[s], k0, cur.m0);
-                tma_load_2d(st + x2::kPlaneBytes, &tmap_lo, &bars->full[s], k0, cur.m0);
-                tma_load_2d(st + 2 * x2::kPlaneBytes, &tmap_w, &bars->full[s], k0, cur.n0);
+                tma_load_2d(st + C::kPlaneBytes, &tmap_lo, &bars->full[s], k0, cur.m0);
+                tma_load_2d(st + 2 * C::kPlaneBytes, &tmap_w, &bars->full[s], k0, cur.n0);
                 issued = g + 1;
             }
             if (*reinterpret_cast<volatile int*>(&bars->abort))
@@ -781,7 +790,7 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
                     return desc0 + static_cast<uint64_t>(((blk % NS) * C::kStageBytes + off) >> 4);
                 };
                 for (int i = 0; i < n; ++i) {  // lo * W^T of the chunk; the very first overwrites D
-                    const uint64_t a = sdesc(g + i, x2::kPlaneBytes), w = sdesc(g + i, 2 * x2::kPlaneBytes);
+                    const uint64_t a = sdesc(g + i, C::kPlaneBytes), w = sdesc(g + i, 2 * C::kPlaneBytes);
 #pragma unroll
                     for (int j = 0; j < BK / 16; ++j)
                         umma_f16_by(leader, d, a + 2 * j, w + 2 * j, C::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
@@ -792,7 +801,7 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
                 const int n2 = (P.nk - kb2 < CH) ? P.nk - kb2 : CH;
                 bool ready2 = true;
                 for (int i = 0; i < n; ++i) {  // hi * W^T; the first scales D by 2^-10 on input
-                    const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * x2::kPlaneBytes);
+                    const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * C::kPlaneBytes);
                     if (i == n - 1 && g2 < total)
                         ready2 = test_chunk(g2, c2, n2);
 #pragma unroll
@@ -1403,11 +1412,11 @@ comp_status_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t
     return COMP_OK;
 }
 
-template <int BN, int NS, int CH>
+template <int BN, int NS, int CH, int AR = BM>
 comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                            const DeviceInfo& dev, cudaStream_t stream)
 {
-    using C = x2::Cfg<BN, NS, CH>;
+    using C = x2::Cfg<BN, NS, CH, AR>;
     static std::mutex mu;
     static bool done[64] = {};
     {
@@ -1415,7 +1424,7 @@ comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const C
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (!done[dev.device]) {
-            if (cudaFuncSetAttribute(comp_f16x2_kernel<BN, NS, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(comp_f16x2_kernel<BN, NS, CH, AR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(C::kSmem)) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return COMP_ERR_CUDA;
@@ -1425,7 +1434,7 @@ comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const C
     }
     const int tiles = P.tiles_m * P.tiles_n;
     const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-    return launch_pdl(comp_f16x2_kernel<BN, NS, CH>, grid, x2::kThreads, C::kSmem, stream, th, tl, tw, P);
+    return launch_pdl(comp_f16x2_kernel<BN, NS, CH, AR>, grid, x2::kThreads, C::kSmem, stream, th, tl, tw, P);
 }
 
 template <int BN, int NS, int CH>
@@ -1566,15 +1575,48 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     P.tiles_n = static_cast<int>((N + bn - 1) / bn);
     if (static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
         return COMP_ERR_INVALID_VALUE;
-    if (!encode_2d(&th, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hi, K, M, BK, BM) ||
-        !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, BM) ||
+    // at most 32 rows (decode-like shapes): 32-row boxes, 7 to 10 stages in flight
+    const uint32_t box_rows = M <= 32 ? 32u : static_cast<uint32_t>(BM);
+    if (!encode_2d(&th, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hi, K, M, BK, box_rows) ||
+        !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, box_rows) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn)))
         return COMP_ERR_CUDA;
+    if (M <= 32) {
+        if (bn == 192)
+            return launch_x2_bn<192, 7, 2, 32>(th, tl, tw, P, dev, stream);
+        if (bn == 128)
+            return launch_x2_bn<128, 9, 2, 32>(th, tl, tw, P, dev, stream);
+        return launch_x2_bn<96, 10, 2, 32>(th, tl, tw, P, dev, stream);
+    }
     if (bn == 192)
         return launch_x2_bn<192, 4, 2>(th, tl, tw, P, dev, stream);
     if (bn == 128)
         return launch_x2_bn<128, 4, 2>(th, tl, tw, P, dev, stream);
     return launch_x2_bn<96, 4, 2>(th, tl, tw, P, dev, stream);
+}
+
+namespace {
+
+// One thread waits, through the same bounded wait as the pipelines, on a
+// barrier that nothing completes; the wait gives up and records the code.
+__global__ void check_wait_timeout_kernel()
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        (void)wait_bounded(&bar, 0, &abort_flag, COMP_FAULT_CHECK_TIMEOUT);
+    }
+}
+
+}  // namespace
+
+comp_status_t launch_check_wait_timeout(cudaStream_t stream)
+{
+    check_wait_timeout_kernel<<<1, 32, 0, stream>>>();
+    return launch_status();
 }
 
 comp_status_t read_and_clear_fault(cudaStream_t stream, uint32_t* where)

@@ -35,6 +35,9 @@ bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t
 comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
                                 int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream);
 
+// One thread runs a bounded wait that cannot succeed (comp_check_wait_timeout).
+comp_status_t launch_check_wait_timeout(cudaStream_t stream);
+
 // Reads and clears the fault word of the tensor-core kernels (after the stream
 // has been synchronised).
 comp_status_t read_and_clear_fault(cudaStream_t stream, uint32_t* where);

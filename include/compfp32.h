@@ -210,6 +210,19 @@ comp_status_t comp_gemm_f32x16_noalloc(const float* x, const uint16_t* W, float*
  */
 comp_status_t comp_device_status(comp_stream_t stream, uint32_t* where);
 
+/*
+ * comp_check_wait_timeout — diagnostic for the path above.  Enqueues one thread
+ * that waits, with the library's bounded wait, on a barrier that nothing ever
+ * completes.  After about a second the wait gives up, records fault code
+ * COMP_FAULT_CHECK_TIMEOUT and the kernel exits.  comp_device_status then
+ * returns COMP_ERR_TIMEOUT with that code, and the context stays usable.  The
+ * pages have no counterpart; the call exists so that the reporting of a stuck
+ * pipeline wait can be tested without faulting or hanging a GPU.  Returns
+ * COMP_ERR_UNSUPPORTED_DEVICE off sm_103 and COMP_ERR_LAUNCH if the launch fails.
+ */
+#define COMP_FAULT_CHECK_TIMEOUT 0x0F01u
+comp_status_t comp_check_wait_timeout(comp_stream_t stream);
+
 /* Human-readable name of a status code (a static string). */
 const char* comp_status_string(comp_status_t status);
 
