@@ -77,7 +77,8 @@ def _compile(src: str) -> tuple[str, str]:
 # Kernels that move registers between warpgroups with setmaxnreg assume this
 # launch register count; a different count could make setmaxnreg.inc wait
 # forever, so the build refuses it.
-SETMAXNREG_KERNELS = {"comp_gemm_kernel": 96, "comp_f16x2_kernel": 168, "comp_f16x2_pair_kernel": 168}
+SETMAXNREG_KERNELS = {"comp_gemm_kernel": 96, "comp_f16x2_kernel": 168, "comp_f16x2_pair_kernel": 168,
+                      "comp_f16x2_splitk_kernel": 168}
 
 
 def _check_register_budget(ptxas_log: str) -> None:

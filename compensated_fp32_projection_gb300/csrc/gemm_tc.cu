@@ -641,7 +641,9 @@ static_assert(128 * kCtrlRegs + 32 * kPromoters * kPromoRegs <= kThreads * kLaun
 // rows AR..127 read whatever follows inside the same stage, and since each
 // output row depends only on its own A row, those garbage rows only produce
 // outputs that are never stored.
-template <int BN, int NS, int CH, int AR = BM>
+// KS: CTAs of a cluster that split K for the same tile (1: no split); their
+// partial sums are added in rank order through the leader's shared memory.
+template <int BN, int NS, int CH, int AR = BM, int KS = 1>
 struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
     static_assert(NS >= 2 && CH >= 1 && CH <= NS, "stages");
@@ -651,7 +653,11 @@ struct Cfg {
     static constexpr uint32_t kStageBytes = 2 * kPlaneBytes + kWBytes;  // hi | lo | W
     static_assert(kStageBytes % 1024 == 0, "stage alignment of the 128-byte swizzle");
     static_assert(kPlaneBytes + BM * BK * 2 <= kStageBytes, "the 128-row read of the lo plane stays in its stage");
-    static constexpr size_t kSmem = 1024 + NS * kStageBytes + 256;
+    static_assert(KS == 1 || (KS <= 8 && AR == 32), "split K serves problems of at most 32 rows");
+    static constexpr int kRedStride = BN / 2 + 4;  // floats per row of a reduction half (padded)
+    static constexpr uint32_t kRedBytes = KS > 1 ? 2u * 32u * kRedStride * 4u : 0u;
+    static constexpr uint32_t kBarBytes = 512;
+    static constexpr size_t kSmem = 1024 + NS * kStageBytes + kBarBytes + kRedBytes;
     static_assert(kSmem <= 232448, "shared memory");
     static constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
     static constexpr int kHalf = BN / 2;
@@ -664,6 +670,8 @@ struct Barriers {
     uint64_t dfull[2];        // accumulator buffer holds a finished chunk
     uint64_t dfree[2];        // promotion warps have read the accumulator buffer
     uint64_t drain;
+    uint64_t red_full[2];  // leader: a peer's partial sums for one column half are in the buffer
+    uint64_t red_go[2];    // peer: the leader's buffer for one column half is free for this peer
     uint32_t tmem_base;
     int abort;
 };
@@ -674,25 +682,36 @@ constexpr uint32_t kFaultX2Producer = 0x501;
 constexpr uint32_t kFaultX2MmaFull = 0x502;
 constexpr uint32_t kFaultX2MmaFree = 0x503;
 constexpr uint32_t kFaultX2Promote = 0x504;
+constexpr uint32_t kFaultX2Reduce = 0x505;
 
-template <int BN, int NS, int CH, int AR>
-__global__ void __launch_bounds__(x2::kThreads, 1)
-    comp_f16x2_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
-                      const __grid_constant__ CUtensorMap tmap_w, const Problem P)
+// The body of the single-CTA-tile product kernels.  With KS > 1 the CTAs of a
+// cluster of KS split K for the same tile: rank r takes the contiguous K blocks
+// [r nk / KS, (r + 1) nk / KS), and at the tile end the ranks' FP32 partial
+// sums are added in rank order in the leader (deterministic, no atomics, no
+// global scratch).  Split K is used for problems of at most 32 rows, whose
+// valid rows all sit in TMEM lanes 0..31 (promotion warps 4 and 8).
+template <int BN, int NS, int CH, int AR, int KS>
+__device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, const CUtensorMap& tmap_lo,
+                                                const CUtensorMap& tmap_w, const Problem& P)
 {
-    using C = x2::Cfg<BN, NS, CH, AR>;
+    using C = x2::Cfg<BN, NS, CH, AR, KS>;
     static_assert(NS <= x2::kMaxStages, "stages");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     x2::Barriers* bars = reinterpret_cast<x2::Barriers*>(smem + NS * C::kStageBytes);
-    static_assert(sizeof(x2::Barriers) <= 256, "barrier area");
+    static_assert(sizeof(x2::Barriers) <= C::kBarBytes, "barrier area");
+    float* redbuf = reinterpret_cast<float*>(smem + NS * C::kStageBytes + C::kBarBytes);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    const int rank = KS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int group = static_cast<int>(blockIdx.x) / KS;  // this CTA's cluster (its tiles)
+    const int groups = static_cast<int>(gridDim.x) / KS;
+    const int kb_lo = rank * P.nk / KS;                    // this CTA's K blocks of every tile
+    const int nkr = (rank + 1) * P.nk / KS - kb_lo;
     const int num_tiles = P.tiles_m * P.tiles_n;
-    const int my_tiles =
-        static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
-    const int total = my_tiles * P.nk;
+    const int my_tiles = group < num_tiles ? (num_tiles - 1 - group) / groups + 1 : 0;
+    const int total = my_tiles * nkr;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -704,6 +723,10 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
             mbar_init(&bars->dfree[b], x2::kPromoters);
         }
         mbar_init(&bars->drain, 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&bars->red_full[h], 1);
+            mbar_init(&bars->red_go[h], 1);
+        }
         bars->abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -717,6 +740,8 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (KS > 1)
+        cluster_sync();  // every CTA's barriers initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
@@ -726,19 +751,23 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
             // ---------------- TMA producer: hi, lo and W boxes per K block ----------------
             int issued = 0;
             grid_dependency_wait();  // the planes come from the previous kernel of the stream
-            Cursor<BN> cur;
-            cur.start(P);
-            for (int g = 0; g < total; ++g, cur.next(P)) {
+            int t = group, kb = 0;
+            for (int g = 0; g < total; ++g) {
                 const int s = g % NS;
                 if (g >= NS && !wait_bounded(&bars->empty[s], ((g / NS) - 1) & 1, &bars->abort, kFaultX2Producer))
                     break;
                 uint8_t* st = smem + s * C::kStageBytes;
-                const int k0 = cur.kb * BK;
+                const int k0 = (kb_lo + kb) * BK;
+                const int m0 = tile_m(t, P) * BM, n0 = tile_n(t, P) * BN;
                 mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
-                tma_load_2d(st, &tmap_hi, &bars->full[s], k0, cur.m0);
-                tma_load_2d(st + C::kPlaneBytes, &tmap_lo, &bars->full[s], k0, cur.m0);
-                tma_load_2d(st + 2 * C::kPlaneBytes, &tmap_w, &bars->full[s], k0, cur.n0);
+                tma_load_2d(st, &tmap_hi, &bars->full[s], k0, m0);
+                tma_load_2d(st + C::kPlaneBytes, &tmap_lo, &bars->full[s], k0, m0);
+                tma_load_2d(st + 2 * C::kPlaneBytes, &tmap_w, &bars->full[s], k0, n0);
                 issued = g + 1;
+                if (++kb == nkr) {
+                    kb = 0;
+                    t += groups;
+                }
             }
             if (*reinterpret_cast<volatile int*>(&bars->abort))
                 for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
@@ -779,7 +808,7 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
                 return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             };
             int g = 0, c = 0, kb = 0;
-            int n = (P.nk < CH) ? P.nk : CH;  // blocks in this chunk (chunks stay inside a tile)
+            int n = (nkr < CH) ? nkr : CH;  // blocks in this chunk (chunks stay inside a tile)
             bool ok = total == 0 || wait_chunk(0, 0, n);
             while (g < total && ok) {
                 const int b = c & 1;
@@ -797,8 +826,8 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
                 }
                 // the next chunk's coordinates
                 const int g2 = g + n, c2 = c + 1;
-                const int kb2 = (kb + n == P.nk) ? 0 : kb + n;
-                const int n2 = (P.nk - kb2 < CH) ? P.nk - kb2 : CH;
+                const int kb2 = (kb + n == nkr) ? 0 : kb + n;
+                const int n2 = (nkr - kb2 < CH) ? nkr - kb2 : CH;
                 bool ready2 = true;
                 for (int i = 0; i < n; ++i) {  // hi * W^T; the first scales D by 2^-10 on input
                     const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * C::kPlaneBytes);
@@ -837,10 +866,73 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < C::kHalf; ++i)
             R[i] = 0.0f;
+        // Split-K reduction of one finished tile, for the warps of lane quarter 0
+        // (one per column half).  Peers, in rank order, wait for the leader's go,
+        // store their sums into the leader's buffer and publish them (release at
+        // cluster scope); the leader adds each peer's sums in rank order.
+        auto reduce_tile = [&](int tt) -> bool {
+            float* buf = redbuf + wh * 32 * C::kRedStride + lane * C::kRedStride;
+            if (rank == 0) {
+                for (int p = 1; p < KS; ++p) {
+                    if (lane == 0)
+                        mbar_arrive_release_cluster(mapa_shared(&bars->red_go[wh], static_cast<uint32_t>(p)));
+                    bool ok = true;
+                    if (lane == 0) {
+                        const uint32_t parity = static_cast<uint32_t>(tt * (KS - 1) + p - 1) & 1u;
+                        const long long start = clock64();
+                        while (!mbar_try_wait_acquire_cluster(&bars->red_full[wh], parity)) {
+                            if (*reinterpret_cast<volatile int*>(&bars->abort) || clock64() - start > kWaitLimit) {
+                                atomicCAS(&g_fault_word, 0u, kFaultX2Reduce);
+                                *reinterpret_cast<volatile int*>(&bars->abort) = 1;
+                                ok = false;
+                                break;
+                            }
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0))
+                        return false;
+                    (void)mbar_try_wait_acquire_cluster(&bars->red_full[wh], static_cast<uint32_t>(tt * (KS - 1) + p - 1) & 1u);
+#pragma unroll
+                    for (int i = 0; i < C::kHalf; i += 4) {
+                        const float4 v = *reinterpret_cast<const float4*>(buf + i);
+                        R[i] = __fadd_rn(R[i], v.x);
+                        R[i + 1] = __fadd_rn(R[i + 1], v.y);
+                        R[i + 2] = __fadd_rn(R[i + 2], v.z);
+                        R[i + 3] = __fadd_rn(R[i + 3], v.w);
+                    }
+                    __syncwarp();
+                }
+            } else {
+                bool ok = true;
+                if (lane == 0) {
+                    const long long start = clock64();
+                    while (!mbar_try_wait_acquire_cluster(&bars->red_go[wh], static_cast<uint32_t>(tt) & 1u)) {
+                        if (*reinterpret_cast<volatile int*>(&bars->abort) || clock64() - start > kWaitLimit) {
+                            atomicCAS(&g_fault_word, 0u, kFaultX2Reduce);
+                            *reinterpret_cast<volatile int*>(&bars->abort) = 1;
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0))
+                    return false;
+                (void)mbar_try_wait_acquire_cluster(&bars->red_go[wh], static_cast<uint32_t>(tt) & 1u);
+                const uint32_t dst = mapa_shared(buf, 0);
+#pragma unroll
+                for (int i = 0; i < C::kHalf; i += 4)
+                    st_cluster_v4(dst + 4u * i, R[i], R[i + 1], R[i + 2], R[i + 3]);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_release_cluster(mapa_shared(&bars->red_full[wh], 0));
+            }
+            return true;
+        };
         int g = 0, c = 0, kb = 0;
-        int t = static_cast<int>(blockIdx.x);
+        int t = group;
+        int tt = 0;  // tiles finished by this CTA
         while (g < total) {
-            const int n = (P.nk - kb < CH) ? P.nk - kb : CH;
+            const int n = (nkr - kb < CH) ? nkr - kb : CH;
             const int b = c & 1;
             // one warp polls the barrier; the others wait at a named barrier
             // (no shared-memory traffic) and read the verdict from the abort flag
@@ -868,38 +960,66 @@ __global__ void __launch_bounds__(x2::kThreads, 1)
             g += n;
             ++c;
             kb += n;
-            if (kb == P.nk) {
-                // tile finished: R holds y[m, nb .. nb + BN/2) for this thread's row m
-                const int64_t m = static_cast<int64_t>(tile_m(t, P)) * BM + wq * 32 + lane;
-                const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
-                if (m < P.M) {
-                    float* yrow = P.y + m * P.N;
-                    if (P.vec_y && nb + C::kHalf <= P.N) {
+            if (kb == nkr) {
+                // tile finished: R holds this CTA's sums for y[m, nb .. nb + BN/2), m this thread's row
+                if (KS > 1 && wq == 0) {
+                    // rows 0..31 (the only valid rows here) are in lane quarter 0.  A
+                    // failed reduction leaves the abort flag raised; every promotion
+                    // warp then leaves at the next chunk's wait, together.
+                    (void)reduce_tile(tt);
+                }
+                if (KS == 1 || (rank == 0 && wq == 0)) {
+                    const int64_t m = static_cast<int64_t>(tile_m(t, P)) * BM + wq * 32 + lane;
+                    const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
+                    if (m < P.M && *reinterpret_cast<volatile int*>(&bars->abort) == 0) {
+                        float* yrow = P.y + m * P.N;
+                        if (P.vec_y && nb + C::kHalf <= P.N) {
 #pragma unroll
-                        for (int i = 0; i < C::kHalf; i += 4)
-                            *reinterpret_cast<float4*>(yrow + nb + i) = make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
-                    } else {
+                            for (int i = 0; i < C::kHalf; i += 4)
+                                *reinterpret_cast<float4*>(yrow + nb + i) =
+                                    make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < C::kHalf; ++i)
-                            if (nb + i < P.N)
-                                yrow[nb + i] = R[i];
+                            for (int i = 0; i < C::kHalf; ++i)
+                                if (nb + i < P.N)
+                                    yrow[nb + i] = R[i];
+                        }
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < C::kHalf; ++i)
                     R[i] = 0.0f;
+                ++tt;
                 kb = 0;
-                t += static_cast<int>(gridDim.x);
+                t += groups;
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if (KS > 1)
+        cluster_sync();  // no CTA leaves while another may still write its buffer or barriers
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+template <int BN, int NS, int CH, int AR>
+__global__ void __launch_bounds__(x2::kThreads, 1)
+    comp_f16x2_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
+                      const __grid_constant__ CUtensorMap tmap_w, const Problem P)
+{
+    f16x2_tile_body<BN, NS, CH, AR, 1>(tmap_hi, tmap_lo, tmap_w, P);
+}
+
+template <int BN, int NS, int CH, int AR, int KS>
+__global__ void __cluster_dims__(KS, 1, 1) __launch_bounds__(x2::kThreads, 1)
+    comp_f16x2_splitk_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
+                             const __grid_constant__ CUtensorMap tmap_w, const Problem P)
+{
+    f16x2_tile_body<BN, NS, CH, AR, KS>(tmap_hi, tmap_lo, tmap_w, P);
 }
 
 // ---------------------------------------------------------------------------
@@ -1412,6 +1532,46 @@ comp_status_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t
     return COMP_OK;
 }
 
+template <int BN, int NS, int CH, int AR, int KS>
+comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+                               const DeviceInfo& dev, cudaStream_t stream)
+{
+    using C = x2::Cfg<BN, NS, CH, AR, KS>;
+    static std::mutex mu;
+    static int clusters[64] = {};  // co-resident clusters per device, 0 = not yet known
+    int nc;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev.device < 0 || dev.device >= 64)
+            return COMP_ERR_CUDA;
+        if (clusters[dev.device] == 0) {
+            if (cudaFuncSetAttribute(comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(C::kSmem)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return COMP_ERR_CUDA;
+            }
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count / KS * KS), 1, 1);
+            cfg.blockDim = dim3(x2::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = C::kSmem;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS>, &cfg) !=
+                    cudaSuccess ||
+                n <= 0) {
+                (void)cudaGetLastError();
+                n = dev.sm_count / KS;
+            }
+            clusters[dev.device] = n;
+        }
+        nc = clusters[dev.device];
+    }
+    const int tiles = P.tiles_m * P.tiles_n;
+    const int grid = KS * (tiles < nc ? tiles : nc);
+    return launch_pdl(comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS>, grid, x2::kThreads, C::kSmem, stream, th, tl, tw,
+                      P);
+}
+
 template <int BN, int NS, int CH, int AR = BM>
 comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                            const DeviceInfo& dev, cudaStream_t stream)
@@ -1570,7 +1730,16 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
         return bn == 224 ? launch_pair_bn<224, 4, 2>(th, tl, tw, ty, P, dev, stream)
                          : launch_pair_bn<256, 4, 2>(th, tl, tw, ty, P, dev, stream);
     }
-    const int bn = pick_bn_x2(M, N, dev.sm_count);
+    // at most 32 rows and few tiles: split K over clusters of 2 or 4 CTAs
+    int ks = 1;
+    if (M <= 32) {
+        const int64_t t192 = (N + 191) / 192;
+        if (t192 * 4 <= dev.sm_count && P.nk >= 16)
+            ks = 4;
+        else if (t192 * 2 <= dev.sm_count && P.nk >= 8)
+            ks = 2;
+    }
+    const int bn = ks > 1 ? 192 : pick_bn_x2(M, N, dev.sm_count);
     P.tiles_m = static_cast<int>((M + BM - 1) / BM);
     P.tiles_n = static_cast<int>((N + bn - 1) / bn);
     if (static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
@@ -1581,6 +1750,10 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
         !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, box_rows) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn)))
         return COMP_ERR_CUDA;
+    if (ks == 4)
+        return launch_x2_splitk<192, 6, 2, 32, 4>(th, tl, tw, P, dev, stream);
+    if (ks == 2)
+        return launch_x2_splitk<192, 6, 2, 32, 2>(th, tl, tw, P, dev, stream);
     if (M <= 32) {
         if (bn == 192)
             return launch_x2_bn<192, 7, 2, 32>(th, tl, tw, P, dev, stream);

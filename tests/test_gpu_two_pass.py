@@ -223,7 +223,13 @@ def test_device_status_clean(pkg):
 
 # both product kernels on every tile shape: one CTA per 128-row tile (1) and
 # CTA pairs per 256-row tile (2)
-@pytest.mark.parametrize("shape", SHAPES + [(2048, 2048, 256), (2000, 2001, 136), (300, 4096, 64)],
+# (16, 8000, 1024), (32, 1000, 520): at most 32 rows, K split over clusters of
+# 2 CTAs (the second with 9 K blocks, split 4 + 5); (32, 2048, 2048) and
+# (17, 260, 4096): clusters of 4
+SPLIT_K = [(16, 8000, 1024), (32, 1000, 520), (32, 2048, 2048)]
+
+
+@pytest.mark.parametrize("shape", SHAPES + SPLIT_K + [(2048, 2048, 256), (2000, 2001, 136), (300, 4096, 64)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("variant", [1, 2])
 def test_product_kernels(pkg, orc, shape, variant):
@@ -255,3 +261,16 @@ def test_product_variant_out_of_range(pkg):
     h = torch.zeros(8, 64, dtype=torch.float16, device="cuda")
     with pytest.raises(CompError):
         pkg.comp_gemm_f16x2_variant(h, h.clone(), torch.zeros(16, 64, dtype=torch.float16, device="cuda"), 3)
+
+
+@pytest.mark.parametrize("shape", SPLIT_K, ids=lambda s: "x".join(map(str, s)))
+def test_split_k_deterministic(pkg, shape):
+    # the partial sums of the K ranges are added in a fixed order: bit-identical reruns
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=11)
+    hi, lo = pkg.comp_split_f32(x.cuda())
+    y1 = pkg.comp_gemm_f16x2(hi, lo, W.cuda())
+    y2 = pkg.comp_gemm_f16x2(hi, lo, W.cuda())
+    assert torch.equal(bits(y1), bits(y2))
