@@ -364,26 +364,48 @@ def run_ours(args):
     flops = float(s.flops)
     value = world * flops / (ms * 1e-3) / 1e12
 
-    # end to end through the public API: pinned host inputs in, result out, every step
+    # end to end through the public API, pipelined like a serving loop: step i's
+    # inputs go up on one copy stream while step i-1 computes and step i-2's
+    # result comes down on another.  Every step still copies its own x and W
+    # from pinned host memory and its own y back; two buffer sets, each reused
+    # only after its previous result has left the device.
     x_h = x_cpu.pin_memory()
     W_h = W_cpu.pin_memory()
-    y_h = torch.empty((s.M, s.N), dtype=torch.float32).pin_memory()
+    y_h = [torch.empty((s.M, s.N), dtype=torch.float32).pin_memory() for _ in range(2)]
+    bufs = [(torch.empty_like(x), torch.empty_like(W), torch.empty_like(y), torch.empty_like(ws)) for _ in range(2)]
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
+    def run_e2e(nsteps):
+        done_out = [None, None]
+        for i in range(nsteps):
+            xb, Wb, yb, wsb = bufs[i % 2]
+            if done_out[i % 2] is not None:
+                s_in.wait_event(done_out[i % 2])
+            with torch.cuda.stream(s_in):
+                xb.copy_(x_h, non_blocking=True)
+                Wb.copy_(W_h, non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+            s_comp.wait_event(ev_in)
+            pkg.comp_gemm_f32x16_ws(xb, Wb, yb, workspace=wsb, stream=s_comp)
+            ev_c = torch.cuda.Event()
+            ev_c.record(s_comp)
+            s_out.wait_event(ev_c)
+            with torch.cuda.stream(s_out):
+                y_h[i % 2].copy_(yb, non_blocking=True)
+            ev_o = torch.cuda.Event()
+            ev_o.record(s_out)
+            done_out[i % 2] = ev_o
+        return done_out
+
     e2e_steps = max(3, min(args.steps, 30))
-    for _ in range(2):
-        x.copy_(x_h, non_blocking=True)
-        W.copy_(W_h, non_blocking=True)
-        pkg.comp_gemm_f32x16_ws(x, W, y, workspace=ws)
-        y_h.copy_(y, non_blocking=True)
+    run_e2e(2)
     barrier()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        x.copy_(x_h, non_blocking=True)
-        W.copy_(W_h, non_blocking=True)
-        pkg.comp_gemm_f32x16_ws(x, W, y, workspace=ws)
-        y_h.copy_(y, non_blocking=True)
-    b.record(stream)
+    a.record(s_in)
+    run_e2e(e2e_steps)
+    b.record(s_out)  # after the last result's copy, which depends on every earlier step
     barrier()
     e2e_ms = a.elapsed_time(b) / e2e_steps
     if dist is not None:
@@ -467,6 +489,8 @@ def run_ours(args):
             "unit": UNIT,
             "h2d_bytes_per_step": 4 * s.M * s.K + 2 * s.N * s.K,
             "d2h_bytes_per_step": 4 * s.M * s.N,
+            "pipeline": "comp_gemm_f32x16_ws on a compute stream; inputs up and results down on two copy streams, "
+                        "two buffer sets",
         },
         "gpu_launches": 2 * args.steps,
         "kernels": {
