@@ -437,6 +437,32 @@ def run_ours(args):
     simt_tflops = flops / (mean * 1e-3) / 1e12
     del xs, hi, lo, a32, b32, o32
 
+    # the other configurations (parity cases), each through the workspace entry
+    # point with the same flush; roofline time t* = max(tensor work / tensor peak,
+    # algorithmic bytes / HBM peak)
+    peaks_now, _ = load_peaks()
+    others = {}
+    for name in ("tiny", "encoder", "skinny", "nonaligned"):
+        so = workloads.SHAPES[name]
+        xo_c, Wo_c = workloads.make_inputs(name)
+        xo, Wo = xo_c.to(dev), Wo_c.to(dev)
+        yo = torch.empty((so.M, so.N), dtype=torch.float32, device=dev)
+        wso = torch.empty(max(1, pkg.comp_gemm_workspace_bytes(so.M, so.K)), dtype=torch.uint8, device=dev)
+        med, mean = time_kernel(lambda: pkg.comp_gemm_f32x16_ws(xo, Wo, yo, workspace=wso), flush, stream, 20)
+        byts = 4 * so.M * so.K + 2 * so.N * so.K + 4 * so.M * so.N
+        t_star = max(4.0 * so.M * so.N * so.K / (peaks_now["bf16_tflops"] * 1e12), byts / (peaks_now["hbm_gbs"] * 1e9))
+        two_pass = so.K % 8 == 0
+        others[name] = {
+            "M": so.M, "N": so.N, "K": so.K,
+            "us": med * 1e3,
+            "eff_TFLOP/s": 2.0 * so.M * so.N * so.K / (med * 1e-3) / 1e12,
+            "GB/s": byts / (med * 1e-3) / 1e9,
+            "frac_of_roofline": t_star / (med * 1e-3),
+            "bound": "tensor" if t_star == 4.0 * so.M * so.N * so.K / (peaks_now["bf16_tflops"] * 1e12) else "hbm",
+            "path": ("split + product kernel" if two_pass else "fused kernel (K % 8 != 0)"),
+        }
+        del xo, Wo, yo, wso
+
     if rank != 0:
         if dist is not None:
             dist.barrier()
@@ -503,6 +529,7 @@ def run_ours(args):
             "comp_merge_f32": {"n": n, "GB/s": merge_gbs, "frac_of_hbm": merge_gbs / peaks["hbm_gbs"]},
             "comp_gemm_f32_simt": {"TFLOP/s": simt_tflops},
         },
+        "other_configs": others,
     }
     if clocks is not None:
         line["clocks"] = clocks

@@ -26,6 +26,7 @@ __all__ = [
     "comp_gemm_f16x2_variant",
     "comp_gemm_f32x16_ws",
     "comp_gemm_workspace_bytes",
+    "comp_gemm_workspace_bytes_mnk",
     "comp_gemm_f32x16_noalloc",
     "device_status",
     "status_string",
@@ -154,14 +155,22 @@ def comp_gemm_workspace_bytes(M, K):
     return int(_native.load().comp_gemm_workspace_bytes(int(M), int(K)))
 
 
+def comp_gemm_workspace_bytes_mnk(M, N, K):
+    """Workspace bytes of the two-pass form for any K and W alignment (4*M*Kp + 2*N*Kp, Kp = K rounded up to 8)."""
+    return int(_native.load().comp_gemm_workspace_bytes_mnk(int(M), int(N), int(K)))
+
+
 def comp_gemm_f32x16_ws(x, W, y=None, workspace=None, stream=None):
     """comp_gemm_f32x16 with a device workspace (uint8 tensor); with enough room
-    (comp_gemm_workspace_bytes) it runs the two-pass form: split once, then the
-    two products and the merge."""
+    it runs the two-pass form: split once, then the two products and the merge.
+    Allocated here when not given: comp_gemm_workspace_bytes(M, K) when K is a
+    multiple of 8 and W is 16-byte aligned, else comp_gemm_workspace_bytes_mnk."""
     torch = _torch()
     M, N, K, y = _gemm_args(x, W, y)
     if workspace is None:
-        workspace = torch.empty(comp_gemm_workspace_bytes(M, K), dtype=torch.uint8, device=x.device)
+        aligned = K % 8 == 0 and W.data_ptr() % 16 == 0
+        nbytes = comp_gemm_workspace_bytes(M, K) if aligned else comp_gemm_workspace_bytes_mnk(M, N, K)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
     if workspace.device.type != "cuda" or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA tensor")
     nbytes = workspace.numel() * workspace.element_size()

@@ -201,6 +201,18 @@ int64_t comp_gemm_workspace_bytes(int64_t M, int64_t K)
     return 4 * mk;
 }
 
+int64_t comp_gemm_workspace_bytes_mnk(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 0 || N < 0 || K < 0 || K > INT64_MAX - 8)
+        return 0;
+    const int64_t Kp = (K + 7) / 8 * 8;
+    int64_t mk = 0, nk = 0;
+    if (!mul_ok(M, Kp, &mk) || !mul_ok(N, Kp, &nk) || mk > INT64_MAX / 8 || nk > INT64_MAX / 8 ||
+        4 * mk > INT64_MAX - 2 * nk)
+        return 0;
+    return 4 * mk + 2 * nk;
+}
+
 comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                   void* workspace, int64_t workspace_bytes, comp_stream_t stream)
 {
@@ -210,23 +222,38 @@ comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, i
     const comp_status_t st = check_gemm(x, 4, W, y, M, N, K, s, &dev, &empty);
     if (st != COMP_OK || empty)
         return st;
-    const int64_t need = comp_gemm_workspace_bytes(M, K);
     if (workspace_bytes < 0 || (workspace_bytes > 0 && !workspace))
         return COMP_ERR_INVALID_VALUE;
     if (workspace && workspace_bytes > 0 &&
         (overlap(workspace, workspace_bytes, x, 4 * M * K) || overlap(workspace, workspace_bytes, W, 2 * N * K) ||
          overlap(workspace, workspace_bytes, y, 4 * M * N)))
         return COMP_ERR_INVALID_VALUE;
-    uint16_t* hi = static_cast<uint16_t*>(workspace);
-    uint16_t* lo = hi ? hi + M * K : nullptr;
-    const bool two_pass = workspace && need > 0 && workspace_bytes >= need &&
-                          (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && gemm_f16x2_supported(hi, lo, W, K);
-    if (!two_pass)
-        return launch_gemm_tc(x, W, y, M, N, K, 0, dev, s);
-    const comp_status_t sp = launch_split(x, hi, lo, M * K, dev, s);
-    if (sp != COMP_OK)
-        return sp;
-    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, 0, dev, s);
+    uint16_t* const ws = static_cast<uint16_t*>(workspace);
+    const bool ws_aligned = (reinterpret_cast<uintptr_t>(workspace) & 15u) == 0;
+    // two-pass form on the caller's W: planes [M, K] in the workspace
+    const int64_t need = comp_gemm_workspace_bytes(M, K);
+    if (ws && ws_aligned && need > 0 && workspace_bytes >= need && gemm_f16x2_supported(ws, ws + M * K, W, K)) {
+        const comp_status_t sp = launch_split(x, ws, ws + M * K, M * K, dev, s);
+        if (sp != COMP_OK)
+            return sp;
+        return launch_gemm_f16x2(ws, ws + M * K, W, y, M, N, K, 0, dev, s);
+    }
+    // two-pass form with K padded to a multiple of 8 (any K, any alignment):
+    // planes [M, Kp] and a zero-padded copy of W [N, Kp] in the workspace
+    const int64_t need_p = comp_gemm_workspace_bytes_mnk(M, N, K);
+    if (ws && ws_aligned && need_p > 0 && workspace_bytes >= need_p) {
+        const int64_t Kp = (K + 7) / 8 * 8;
+        uint16_t* hi = ws;
+        uint16_t* lo = ws + M * Kp;
+        uint16_t* wp = ws + 2 * M * Kp;
+        comp_status_t r = launch_split_padded(x, hi, lo, M, K, Kp, dev, s);
+        if (r == COMP_OK)
+            r = launch_pad_rows(W, wp, N, K, Kp, dev, s);
+        if (r != COMP_OK)
+            return r;
+        return launch_gemm_f16x2(hi, lo, wp, y, M, N, Kp, 0, dev, s);
+    }
+    return launch_gemm_tc(x, W, y, M, N, K, 0, dev, s);
 }
 
 comp_status_t comp_check_wait_timeout(comp_stream_t stream)

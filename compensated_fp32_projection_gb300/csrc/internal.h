@@ -20,6 +20,12 @@ comp_status_t current_device(DeviceInfo* info);
 // Launchers (arguments already validated; sizes > 0).
 comp_status_t launch_split(const float* x, uint16_t* hi, uint16_t* lo, int64_t n, const DeviceInfo& dev,
                            cudaStream_t stream);
+// Split into planes [rows, Kp] (Kp >= K, a multiple of 8) with zero padding,
+// and a zero-padded copy of a binary16 matrix into rows of Kp elements.
+comp_status_t launch_split_padded(const float* x, uint16_t* hi, uint16_t* lo, int64_t rows, int64_t K, int64_t Kp,
+                                  const DeviceInfo& dev, cudaStream_t stream);
+comp_status_t launch_pad_rows(const uint16_t* src, uint16_t* dst, int64_t rows, int64_t K, int64_t Kp,
+                              const DeviceInfo& dev, cudaStream_t stream);
 comp_status_t launch_merge(const float* acc_hi, const float* acc_lo, float* y, int64_t n, const DeviceInfo& dev,
                            cudaStream_t stream);
 comp_status_t launch_gemm_simt(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,

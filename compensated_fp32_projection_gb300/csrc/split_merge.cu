@@ -87,6 +87,43 @@ __global__ void __launch_bounds__(kThreads) split_scalar_kernel(const float* __r
     }
 }
 
+// Split of a row-major x [rows, K] into planes with a wider row stride Kp >= K
+// (a multiple of 8, so that their rows start on 16-byte boundaries); the
+// columns K..Kp-1 of both planes are +0, which adds exact zeros to every dot
+// product.  Any alignment of x.
+__global__ void __launch_bounds__(kThreads) split_pad_kernel(const float* __restrict__ x, uint16_t* __restrict__ hi,
+                                                             uint16_t* __restrict__ lo, int64_t rows, int64_t K,
+                                                             int64_t Kp)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t n = rows * Kp;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int64_t r = i / Kp, k = i - r * Kp;
+        uint16_t h = 0, l = 0;
+        if (k < K) {
+            const float v = x[r * K + k];
+            const __half hh = __float2half_rn(v);
+            h = __half_as_ushort(hh);
+            l = __half_as_ushort(__float2half_rn(__fmul_rn(__fsub_rn(v, __half2float(hh)), 1024.0f)));
+        }
+        hi[i] = h;
+        lo[i] = l;
+    }
+}
+
+// Copy of a row-major binary16 matrix [rows, K] into rows of Kp >= K elements,
+// zero-filled past K.
+__global__ void __launch_bounds__(kThreads) pad_rows_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                                            int64_t rows, int64_t K, int64_t Kp)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t n = rows * Kp;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int64_t r = i / Kp, k = i - r * Kp;
+        dst[i] = k < K ? src[r * K + k] : static_cast<uint16_t>(0);
+    }
+}
+
 __device__ __forceinline__ float merge1(float a, float b)
 {
     return __fadd_rn(a, __fmul_rn(b, 0x1p-10f));
@@ -162,6 +199,20 @@ comp_status_t launch_split(const float* x, uint16_t* hi, uint16_t* lo, int64_t n
             return COMP_ERR_LAUNCH;
     }
     return COMP_OK;
+}
+
+comp_status_t launch_split_padded(const float* x, uint16_t* hi, uint16_t* lo, int64_t rows, int64_t K, int64_t Kp,
+                                  const DeviceInfo& dev, cudaStream_t stream)
+{
+    split_pad_kernel<<<grid_for(rows * Kp, dev), kThreads, 0, stream>>>(x, hi, lo, rows, K, Kp);
+    return launch_status();
+}
+
+comp_status_t launch_pad_rows(const uint16_t* src, uint16_t* dst, int64_t rows, int64_t K, int64_t Kp,
+                              const DeviceInfo& dev, cudaStream_t stream)
+{
+    pad_rows_kernel<<<grid_for(rows * Kp, dev), kThreads, 0, stream>>>(src, dst, rows, K, Kp);
+    return launch_status();
 }
 
 comp_status_t launch_merge(const float* acc_hi, const float* acc_lo, float* y, int64_t n, const DeviceInfo& dev,

@@ -161,14 +161,29 @@ comp_status_t comp_gemm_f16x2_variant(const uint16_t* hi, const uint16_t* lo, co
 int64_t comp_gemm_workspace_bytes(int64_t M, int64_t K);
 
 /*
+ * comp_gemm_workspace_bytes_mnk — the workspace comp_gemm_f32x16_ws needs for
+ * the two-pass form whatever K and the alignment of W: with
+ * Kp = K rounded up to a multiple of 8, 4 * M * Kp + 2 * N * Kp bytes (hi and lo
+ * planes [M, Kp] and a zero-padded copy of W [N, Kp]).  0 for a negative or
+ * overflowing size.
+ */
+int64_t comp_gemm_workspace_bytes_mnk(int64_t M, int64_t N, int64_t K);
+
+/*
  * comp_gemm_f32x16_ws — comp_gemm_f32x16 with a caller-provided device
- * workspace.  When the workspace holds comp_gemm_workspace_bytes(M, K) bytes,
- * is 16-byte aligned, x and W are 16-byte aligned and K is a multiple of 8, the
- * call enqueues the two-pass form: comp_split_f32 of x into the workspace (hi
- * plane, then lo plane) and comp_gemm_f16x2.  Otherwise it is exactly
- * comp_gemm_f32x16.  The workspace's contents are overwritten; it must not
- * overlap x, W or y (COMP_ERR_INVALID_VALUE).  Same results within the same
- * tolerance either way.
+ * workspace (16-byte aligned), which must not overlap x, W or y
+ * (COMP_ERR_INVALID_VALUE); its contents are overwritten.  The call enqueues
+ * the two-pass form: comp_split_f32 of x into the workspace, then
+ * comp_gemm_f16x2.
+ *   - K a multiple of 8, W 16-byte aligned, workspace of at least
+ *     comp_gemm_workspace_bytes(M, K): the planes [M, K] (hi, then lo) and
+ *     the caller's W.
+ *   - Otherwise, with at least comp_gemm_workspace_bytes_mnk(M, N, K): the
+ *     planes [M, Kp] with zero columns past K and a zero-padded copy of W
+ *     [N, Kp], Kp = K rounded up to 8.  The added columns contribute exact
+ *     zeros.
+ *   - Otherwise (no or too small a workspace) exactly comp_gemm_f32x16.
+ * Same results within the same tolerance either way; x may have any alignment.
  */
 comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                   void* workspace, int64_t workspace_bytes, comp_stream_t stream);

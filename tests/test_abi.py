@@ -99,6 +99,14 @@ def test_two_pass_argument_errors(lib):
     assert ws(None, None, None, 0, 4, 4, None, 0, None) == 0
 
 
+def test_workspace_bytes_mnk(lib):
+    assert lib.comp_gemm_workspace_bytes_mnk(1000, 771, 1027) == 4 * 1000 * 1032 + 2 * 771 * 1032
+    assert lib.comp_gemm_workspace_bytes_mnk(4096, 4096, 4096) == 4 * 4096 * 4096 + 2 * 4096 * 4096
+    assert lib.comp_gemm_workspace_bytes_mnk(0, 0, 5) == 0
+    assert lib.comp_gemm_workspace_bytes_mnk(-1, 4, 4) == 0
+    assert lib.comp_gemm_workspace_bytes_mnk(1 << 40, 4, 1 << 30) == 0  # overflows
+
+
 def test_workspace_bytes(lib):
     assert lib.comp_gemm_workspace_bytes(4096, 4096) == 4 * 4096 * 4096
     assert lib.comp_gemm_workspace_bytes(0, 77) == 0

@@ -52,17 +52,49 @@ def test_shapes_sampled(pkg, orc, name):
     assert torch.isfinite(y).all()
 
 
-def test_nonaligned_k_takes_the_fused_kernel(pkg, orc):
-    # K = 1027 is not a multiple of 8: the workspace is ignored and the result
-    # is the fused kernel's, bit for bit
+def test_nonaligned_k_takes_the_padded_two_pass_form(pkg, orc):
+    # K = 1027 is not a multiple of 8: with the workspace of
+    # comp_gemm_workspace_bytes_mnk the planes and a copy of W are padded to
+    # K = 1032 with zeros; with a workspace of only 4*M*K the call is exactly
+    # the fused kernel
     from compensated_fp32_projection_gb300 import workloads
 
     x, W = workloads.make_inputs("nonaligned")
-    x, W = x.cuda(), W.cuda()
-    y_ws = pkg.comp_gemm_f32x16_ws(x, W)
-    y_fused = pkg.comp_gemm_f32x16(x, W)
-    assert torch.equal(bits(y_ws), bits(y_fused))
-    check_comp(y_ws, x.cpu(), W.cpu(), orc)
+    M, K = x.shape
+    N = W.shape[0]
+    xd, Wd = x.cuda(), W.cuda()
+    y_pad = pkg.comp_gemm_f32x16_ws(xd, Wd)
+    e_gpu, e_cast = check_comp(y_pad, x, W, orc)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+    small = torch.empty(pkg.comp_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    y_small = pkg.comp_gemm_f32x16_ws(xd, Wd, workspace=small)
+    y_fused = pkg.comp_gemm_f32x16(xd, Wd)
+    assert torch.equal(bits(y_small), bits(y_fused))
+
+
+@pytest.mark.parametrize("shape", [(129, 257, 1027), (3, 5, 7), (300, 520, 1001), (2048, 2048, 333)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_padded_two_pass_shapes(pkg, orc, shape):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=M + N + K, scale=2.0)
+    y = pkg.comp_gemm_f32x16_ws(x.cuda(), W.cuda())
+    check_comp(y, x, W, orc)
+
+
+def test_misaligned_w_takes_the_padded_form(pkg, orc):
+    # K a multiple of 8 but W 2 bytes off a 16-byte boundary: W cannot be read
+    # with the tensor memory accelerator, so it is copied (padded form)
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = 130, 300, 72
+    x, W = workloads.random_case(M, N, K, seed=5)
+    big = torch.empty(N * K + 8, dtype=torch.float16, device="cuda")
+    Wd = big[1:1 + N * K].view(N, K)
+    Wd.copy_(W.cuda())
+    y = pkg.comp_gemm_f32x16_ws(x.cuda(), Wd)
+    check_comp(y, x, W, orc)
 
 
 # K multiples of 8 only (the planes are read with the tensor memory accelerator);
