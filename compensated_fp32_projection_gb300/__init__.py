@@ -130,7 +130,8 @@ def comp_gemm_f16x2(hi, lo, W, y=None, stream=None):
 
 
 def comp_gemm_f16x2_variant(hi, lo, W, variant, y=None, stream=None):
-    """comp_gemm_f16x2 with a chosen kernel (0 auto, 1 one CTA per 128-row tile, 2 CTA pairs)."""
+    """comp_gemm_f16x2 with a chosen kernel (0 auto, 1 one CTA per 128-row tile, 2 CTA pairs,
+    3 operands swapped for M <= 32)."""
     torch = _torch()
     _check(hi, torch.float16, "hi")
     _check(lo, torch.float16, "lo")

@@ -1366,6 +1366,249 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Two-pass product for problems of at most 32 rows, with the operands swapped.
+// The tensor cores compute y^T = W x^T.  The A operand is a 128-row tile of W,
+// so the MMA rows are all used however small M is.  The B operand is the x rows
+// padded to Mp (16 or 32): Mp hi rows, then Mp lo rows, N = 2 Mp.  One MMA
+// therefore reads its 4 KB of W once for both products.  TMEM lane n of a
+// tile holds, for output column n, the hi sums in columns 0..Mp-1 and the lo
+// sums in Mp..2Mp-1.  Each chunk of CH K blocks accumulates fresh, and
+// promotion adds both halves into FP32 registers.  The epilogue merges
+// y = R_hi + rn(2^-10 R_lo) and a warp stores 32 consecutive columns of one
+// row of y per instruction.  With no order between the two products inside an
+// MMA, each stage goes back to the producer right after its block.
+// ---------------------------------------------------------------------------
+namespace swp {
+constexpr int kPromoters = 4;
+constexpr int kThreads = 128 + 32 * kPromoters;  // warpgroup 0: producer, MMA issuer, two idle warps
+constexpr int kTileN = 128;                       // W rows per tile (the MMA's M)
+constexpr int kMaxStages = 12;
+constexpr uint32_t kTmemCols = 128;               // two accumulator buffers of up to 64 columns
+
+template <int MP, int NS, int CH>
+struct Cfg {
+    static_assert(MP == 16 || MP == 32, "padded rows of x");
+    static_assert(NS >= 2 && NS <= kMaxStages && CH >= 1, "pipeline");
+    static constexpr uint32_t kWBytes = kTileN * BK * 2;  // 16 KB
+    static constexpr uint32_t kXBox = MP * BK * 2;        // one plane's Mp rows
+    static constexpr uint32_t kStageBytes = kWBytes + 2 * kXBox;
+    static_assert(kStageBytes % 1024 == 0 && kXBox % 1024 == 0, "128-byte swizzle atoms");
+    static constexpr size_t kSmem = 1024 + NS * kStageBytes + 512;
+    static_assert(kSmem <= 232448, "shared memory");
+    static constexpr int kCols = 2 * MP;  // accumulator columns per buffer
+    static constexpr uint32_t kIdesc = idesc_f16_f32(kTileN, kCols);
+};
+
+struct Barriers {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t dfull[2];
+    uint64_t dfree[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+}  // namespace swp
+
+// Fault codes of the swapped-operand product kernel.
+constexpr uint32_t kFaultSwpProducer = 0x801;
+constexpr uint32_t kFaultSwpMma = 0x802;
+constexpr uint32_t kFaultSwpPromote = 0x803;
+
+template <int MP, int NS, int CH>
+__global__ void __launch_bounds__(swp::kThreads, 1)
+    comp_f16x2_swap_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
+                           const __grid_constant__ CUtensorMap tmap_w, const Problem P)
+{
+    using C = swp::Cfg<MP, NS, CH>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    swp::Barriers* bars = reinterpret_cast<swp::Barriers*>(smem + NS * C::kStageBytes);
+    static_assert(sizeof(swp::Barriers) <= 512, "barrier area");
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int num_tiles = P.tiles_n;  // tiles of 128 columns of y (rows of W)
+    const int my_tiles =
+        static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const int total = my_tiles * P.nk;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->dfull[b], 1);
+            mbar_init(&bars->dfree[b], swp::kPromoters);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmap_hi);
+        tma_prefetch_desc(&tmap_lo);
+        tma_prefetch_desc(&tmap_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, swp::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer: the W tile and the x rows of both planes per K block ----------------
+        int issued = 0;
+        grid_dependency_wait();  // the planes come from the previous kernel of the stream
+        int t = static_cast<int>(blockIdx.x), kb = 0;
+        for (int g = 0; g < total; ++g) {
+            const int s = g % NS;
+            if (g >= NS && !wait_bounded(&bars->empty[s], ((g / NS) - 1) & 1, &bars->abort, kFaultSwpProducer))
+                break;
+            uint8_t* st = smem + s * C::kStageBytes;
+            const int k0 = kb * BK;
+            mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
+            tma_load_2d(st, &tmap_w, &bars->full[s], k0, t * swp::kTileN);
+            tma_load_2d(st + C::kWBytes, &tmap_hi, &bars->full[s], k0, 0);              // rows >= M read as 0
+            tma_load_2d(st + C::kWBytes + C::kXBox, &tmap_lo, &bars->full[s], k0, 0);
+            issued = g + 1;
+            if (++kb == P.nk) {
+                kb = 0;
+                t += static_cast<int>(gridDim.x);
+            }
+        }
+        if (*reinterpret_cast<volatile int*>(&bars->abort))
+            for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
+                drain_wait(&bars->full[g % NS], (g / NS) & 1);
+    } else if (warp == 1) {
+        // ---------------- MMA issuer, one chunk of CH K blocks at a time ----------------
+        // The whole warp runs the loop (warp-uniform descriptors); lane 0 issues.
+        // What chunk (g, c) of n blocks needs: its stages, and from the third
+        // chunk on its accumulator buffer back from promotion; tested ahead,
+        // waited for only when still pending.
+        const uint32_t leader = lane == 0 ? 1u : 0u;
+        const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
+        auto test_chunk = [&](int g, int c, int n) -> bool {
+            bool r = c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1);
+            for (int i = 0; i < n; ++i)
+                r = mbar_test_wait(&bars->full[(g + i) % NS], ((g + i) / NS) & 1) && r;
+            return r;
+        };
+        auto wait_chunk = [&](int g, int c, int n) -> bool {
+            bool ok = true;
+            if (lane == 0) {
+                for (int i = 0; i < n && ok; ++i)
+                    ok = wait_bounded(&bars->full[(g + i) % NS], ((g + i) / NS) & 1, &bars->abort, kFaultSwpMma);
+                if (ok && c >= 2)
+                    ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort, kFaultSwpMma);
+            }
+            return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        };
+        int g = 0, c = 0, kb = 0;
+        int n = (P.nk < CH) ? P.nk : CH;
+        bool ok = total == 0 || wait_chunk(0, 0, n);
+        while (g < total && ok) {
+            const int b = c & 1;
+            tc_fence_after();
+            const uint32_t d = tmem + b * C::kCols;
+            const int g2 = g + n, c2 = c + 1;
+            const int kb2 = (kb + n == P.nk) ? 0 : kb + n;
+            const int n2 = (P.nk - kb2 < CH) ? P.nk - kb2 : CH;
+            bool ready2 = true;
+            for (int i = 0; i < n; ++i) {
+                const uint64_t st = desc0 + static_cast<uint64_t>((((g + i) % NS) * C::kStageBytes) >> 4);
+                const uint64_t a = st, bx = st + (C::kWBytes >> 4);  // A: W tile; B: hi rows then lo rows
+                if (i == n - 1 && g2 < total)
+                    ready2 = test_chunk(g2, c2, n2);
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)
+                    umma_f16_by(leader, d, a + 2 * j, bx + 2 * j, C::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
+                umma_commit_by(leader, &bars->empty[(g + i) % NS]);
+            }
+            umma_commit_by(leader, &bars->dfull[b]);
+            g = g2;
+            c = c2;
+            kb = kb2;
+            n = n2;
+            if (g < total && !ready2)
+                ok = wait_chunk(g, c, n);
+        }
+        if (!ok) {
+            umma_commit_by(leader, &bars->drain);
+            if (lane == 0)
+                drain_wait(&bars->drain, 0);
+            __syncwarp();
+        }
+    } else if (warp >= 4) {
+        // ---------------- promotion and epilogue (lane quarter wq = rows 32 wq .. of the tile) ----------------
+        const int wq = warp - 4;
+        float Rh[MP], Rl[MP];
+#pragma unroll
+        for (int i = 0; i < MP; ++i) {
+            Rh[i] = 0.0f;
+            Rl[i] = 0.0f;
+        }
+        int g = 0, c = 0, kb = 0;
+        int t = static_cast<int>(blockIdx.x);
+        while (g < total) {
+            const int n = (P.nk - kb < CH) ? P.nk - kb : CH;
+            const int b = c & 1;
+            if (warp == 4)
+                (void)lane0_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultSwpPromote);
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * swp::kPromoters) : "memory");
+            if (*reinterpret_cast<volatile int*>(&bars->abort))
+                break;
+            tc_fence_after();
+            uint32_t v[C::kCols];
+#pragma unroll
+            for (int q = 0; q < C::kCols / 16; ++q)
+                tmem_ld16(tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * C::kCols + 16 * q,
+                          *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->dfree[b]);
+#pragma unroll
+            for (int i = 0; i < MP; ++i) {
+                Rh[i] = __fadd_rn(Rh[i], __uint_as_float(v[i]));
+                Rl[i] = __fadd_rn(Rl[i], __uint_as_float(v[MP + i]));
+            }
+            g += n;
+            ++c;
+            kb += n;
+            if (kb == P.nk) {
+                // tile finished: this thread holds column col of y for rows 0..M-1
+                const int64_t col = static_cast<int64_t>(t) * swp::kTileN + wq * 32 + lane;
+                if (col < P.N) {
+#pragma unroll
+                    for (int m = 0; m < MP; ++m)
+                        if (m < P.M)
+                            P.y[m * static_cast<int64_t>(P.N) + col] = __fadd_rn(Rh[m], __fmul_rn(Rl[m], 0x1p-10f));
+                }
+#pragma unroll
+                for (int i = 0; i < MP; ++i) {
+                    Rh[i] = 0.0f;
+                    Rl[i] = 0.0f;
+                }
+                kb = 0;
+                t += static_cast<int>(gridDim.x);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, swp::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1572,6 +1815,30 @@ comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, con
                       P);
 }
 
+template <int MP, int NS, int CH>
+comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+                          const DeviceInfo& dev, cudaStream_t stream)
+{
+    using C = swp::Cfg<MP, NS, CH>;
+    static std::mutex mu;
+    static bool done[64] = {};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev.device < 0 || dev.device >= 64)
+            return COMP_ERR_CUDA;
+        if (!done[dev.device]) {
+            if (cudaFuncSetAttribute(comp_f16x2_swap_kernel<MP, NS, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(C::kSmem)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return COMP_ERR_CUDA;
+            }
+            done[dev.device] = true;
+        }
+    }
+    const int grid = P.tiles_n < dev.sm_count ? P.tiles_n : dev.sm_count;
+    return launch_pdl(comp_f16x2_swap_kernel<MP, NS, CH>, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
+}
+
 template <int BN, int NS, int CH, int AR = BM>
 comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                            const DeviceInfo& dev, cudaStream_t stream)
@@ -1695,7 +1962,7 @@ bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t
 comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
                                 int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream)
 {
-    if (!gemm_f16x2_supported(hi, lo, W, K) || variant < 0 || variant > 2)
+    if (!gemm_f16x2_supported(hi, lo, W, K) || variant < 0 || variant > 3 || (variant == 3 && M > 32))
         return COMP_ERR_INVALID_VALUE;
     // CTA pairs once the output fills about one wave of single-CTA tiles: below
     // that, pipeline fill dominates and the 128-row tiles spread over more SMs.
@@ -1711,6 +1978,22 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     P.vec_y = (N % 4 == 0) && aligned16(y);
     P.tma_y = 0;
     CUtensorMap th{}, tl{}, tw{};
+    // at most 32 rows and at least 32 tiles of 128 columns: operands swapped,
+    // W streams through full 128-row MMAs
+    const int64_t t128 = (N + swp::kTileN - 1) / swp::kTileN;
+    if (variant == 3 || (variant == 0 && M <= 32 && t128 >= 32)) {
+        const uint32_t mp = M <= 16 ? 16u : 32u;
+        P.tiles_m = 1;
+        P.tiles_n = static_cast<int>(t128);
+        if (static_cast<int64_t>(P.tiles_n) * P.nk > INT32_MAX / 2)
+            return COMP_ERR_INVALID_VALUE;
+        if (!encode_2d(&th, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hi, K, M, BK, mp) ||
+            !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, mp) ||
+            !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(swp::kTileN)))
+            return COMP_ERR_CUDA;
+        return mp == 16 ? launch_swap<16, 8, 4>(th, tl, tw, P, dev, stream)
+                        : launch_swap<32, 8, 4>(th, tl, tw, P, dev, stream);
+    }
     if (pairs) {
         // CTA pairs on 256-row tiles
         const int bn = pick_bn_pair(M, N, dev.sm_count / 2);

@@ -37,7 +37,8 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
 // The two products and the merge from split planes (hi, lo: [M, K] FP16).
 // Needs 16-byte aligned hi, lo, W and K % 8 == 0 (else COMP_ERR_INVALID_VALUE).
 bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t K);
-// variant: 0 automatic, 1 one CTA per 128-row tile, 2 CTA pairs on 256-row tiles.
+// variant: 0 automatic, 1 one CTA per 128-row tile, 2 CTA pairs on 256-row
+// tiles, 3 operands swapped (M <= 32).
 comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
                                 int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream);
 

@@ -145,10 +145,12 @@ comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint
 
 /*
  * comp_gemm_f16x2_variant — comp_gemm_f16x2 with the kernel chosen by the
- * caller (testing and measurement): 0 automatic, 1 one CTA per 128-row tile,
- * 2 pairs of CTAs (one cluster, both SMs' tensor cores driven by one
- * instruction stream) per 256-row tile.  Same results within the same
- * tolerance; a variant outside 0..2 is COMP_ERR_INVALID_VALUE.
+ * caller (testing and measurement): 0 automatic, 1 one CTA per 128-row tile
+ * (with K split over clusters when M <= 32 and tiles are few), 2 pairs of CTAs
+ * (one cluster, both SMs' tensor cores driven by one instruction stream) per
+ * 256-row tile, 3 operands swapped (y^T = W x^T with 128 rows of W per tile;
+ * M <= 32 only).  Same results within the same tolerance; a variant outside
+ * 0..3, or 3 with M > 32, is COMP_ERR_INVALID_VALUE.
  */
 comp_status_t comp_gemm_f16x2_variant(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
                                       int64_t N, int64_t K, int variant, comp_stream_t stream);

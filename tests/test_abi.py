@@ -92,7 +92,8 @@ def test_two_pass_argument_errors(lib):
     assert f2(P(4096), P(1 << 16), P(1 << 20), P(4096 + 32), 4, 4, 8, None) == 1  # y overlaps hi
     assert f2(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 1 << 40, 1 << 40, 8, None) == 1
     assert f2(None, None, None, None, 0, 4, 8, None) == 0
-    assert lib.comp_gemm_f16x2_variant(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, 3, None) == 1
+    assert lib.comp_gemm_f16x2_variant(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, 4, None) == 1
+    assert lib.comp_gemm_f16x2_variant(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 33, 4, 8, 3, None) == 1
     assert lib.comp_gemm_f16x2_variant(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, -1, None) == 1
     # comp_gemm_f32x16_ws(x, W, y, M, N, K, workspace, bytes, stream)
     assert ws(P(4096), P(1 << 20), P(1 << 24), -1, 4, 4, P(1 << 26), 64, None) == 1

@@ -263,11 +263,13 @@ SPLIT_K = [(16, 8000, 1024), (32, 1000, 520), (32, 2048, 2048)]
 
 @pytest.mark.parametrize("shape", SHAPES + SPLIT_K + [(2048, 2048, 256), (2000, 2001, 136), (300, 4096, 64)],
                          ids=lambda s: "x".join(map(str, s)))
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 def test_product_kernels(pkg, orc, shape, variant):
     from compensated_fp32_projection_gb300 import workloads
 
     M, N, K = shape
+    if variant == 3 and M > 32:
+        pytest.skip("operands are swapped only for at most 32 rows")
     x, W = workloads.random_case(M, N, K, seed=M * 7 + N * 3 + K, scale=2.0)
     hi, lo = pkg.comp_split_f32(x.cuda())
     y = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), variant)
@@ -292,7 +294,24 @@ def test_product_variant_out_of_range(pkg):
 
     h = torch.zeros(8, 64, dtype=torch.float16, device="cuda")
     with pytest.raises(CompError):
-        pkg.comp_gemm_f16x2_variant(h, h.clone(), torch.zeros(16, 64, dtype=torch.float16, device="cuda"), 3)
+        pkg.comp_gemm_f16x2_variant(h, h.clone(), torch.zeros(16, 64, dtype=torch.float16, device="cuda"), 4)
+    h40 = torch.zeros(40, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(CompError):  # swapped operands need M <= 32
+        pkg.comp_gemm_f16x2_variant(h40, h40.clone(), torch.zeros(16, 64, dtype=torch.float16, device="cuda"), 3)
+
+
+@pytest.mark.parametrize("shape", [(16, 14336, 4096), (32, 4100, 1032), (1, 4096, 64), (17, 5000, 520)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_swapped_operands_full(pkg, orc, shape):
+    # at most 32 rows, many column tiles: the automatic choice is the swapped-operand kernel
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=M * 5 + K, scale=2.0)
+    hi, lo = pkg.comp_split_f32(x.cuda())
+    y = pkg.comp_gemm_f16x2(hi, lo, W.cuda())
+    e_gpu, e_cast = check_comp(y, x, W, orc)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
 
 
 @pytest.mark.parametrize("shape", SPLIT_K, ids=lambda s: "x".join(map(str, s)))
@@ -303,6 +322,6 @@ def test_split_k_deterministic(pkg, shape):
     M, N, K = shape
     x, W = workloads.random_case(M, N, K, seed=11)
     hi, lo = pkg.comp_split_f32(x.cuda())
-    y1 = pkg.comp_gemm_f16x2(hi, lo, W.cuda())
-    y2 = pkg.comp_gemm_f16x2(hi, lo, W.cuda())
+    y1 = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), 1)
+    y2 = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), 1)
     assert torch.equal(bits(y1), bits(y2))
