@@ -1372,30 +1372,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
 // padded to Mp (16 or 32): Mp hi rows, then Mp lo rows, N = 2 Mp.  One MMA
 // therefore reads its 4 KB of W once for both products.  TMEM lane n of a
 // tile holds, for output column n, the hi sums in columns 0..Mp-1 and the lo
-// sums in Mp..2Mp-1.  Each chunk of CH K blocks accumulates fresh, and
-// promotion adds both halves into FP32 registers.  The epilogue merges
-// y = R_hi + rn(2^-10 R_lo) and a warp stores 32 consecutive columns of one
-// row of y per instruction.  With no order between the two products inside an
-// MMA, each stage goes back to the producer right after its block.
+// sums in Mp..2Mp-1.
+//
+// The kernel streams W, about 4 bytes of W per FLOP-pair of output, so its
+// bound is DRAM.  A stage holds BPS consecutive 64-wide K blocks of the tile:
+// the BPS W boxes, then per block its hi and lo boxes side by side (one
+// 2 Mp-row B operand).  Asking for several K blocks of the same W rows at
+// once reads more of each DRAM page per visit than one block per stage.  One
+// stage is one accumulation chunk: it accumulates fresh in one of two TMEM
+// buffers and promotion adds both halves into FP32 registers.  The epilogue
+// merges y = R_hi + rn(2^-10 R_lo); a warp stores 32 consecutive columns of
+// one row of y per instruction.
 // ---------------------------------------------------------------------------
 namespace swp {
 constexpr int kPromoters = 4;
 constexpr int kThreads = 128 + 32 * kPromoters;  // warpgroup 0: producer, MMA issuer, two idle warps
 constexpr int kTileN = 128;                       // W rows per tile (the MMA's M)
-constexpr int kMaxStages = 12;
-constexpr uint32_t kTmemCols = 128;               // two accumulator buffers of up to 64 columns
+constexpr int kMaxStages = 8;
 
-template <int MP, int NS, int CH>
+template <int MP, int BPS, int NS>
 struct Cfg {
     static_assert(MP == 16 || MP == 32, "padded rows of x");
-    static_assert(NS >= 2 && NS <= kMaxStages && CH >= 1, "pipeline");
-    static constexpr uint32_t kWBytes = kTileN * BK * 2;  // 16 KB
-    static constexpr uint32_t kXBox = MP * BK * 2;        // one plane's Mp rows
-    static constexpr uint32_t kStageBytes = kWBytes + 2 * kXBox;
-    static_assert(kStageBytes % 1024 == 0 && kXBox % 1024 == 0, "128-byte swizzle atoms");
+    static_assert(BPS >= 1 && BPS <= 8 && NS >= 2 && NS <= kMaxStages, "pipeline");
+    static constexpr uint32_t kWBox = kTileN * BK * 2;  // 16 KB: one K block of the W tile
+    static constexpr uint32_t kXBox = MP * BK * 2;      // one plane's Mp rows of one K block
+    static constexpr uint32_t kStageBytes = BPS * (kWBox + 2 * kXBox);
+    static_assert(kXBox % 1024 == 0, "128-byte swizzle atoms");
     static constexpr size_t kSmem = 1024 + NS * kStageBytes + 512;
     static_assert(kSmem <= 232448, "shared memory");
-    static constexpr int kCols = 2 * MP;  // accumulator columns per buffer
+    static constexpr int kCols = 2 * MP;               // accumulator columns per buffer
+    static constexpr uint32_t kTmemCols = 2 * kCols;  // two buffers (64 or 128 columns)
     static constexpr uint32_t kIdesc = idesc_f16_f32(kTileN, kCols);
 };
 
@@ -1415,12 +1421,12 @@ constexpr uint32_t kFaultSwpProducer = 0x801;
 constexpr uint32_t kFaultSwpMma = 0x802;
 constexpr uint32_t kFaultSwpPromote = 0x803;
 
-template <int MP, int NS, int CH>
+template <int MP, int BPS, int NS>
 __global__ void __launch_bounds__(swp::kThreads, 1)
     comp_f16x2_swap_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
                            const __grid_constant__ CUtensorMap tmap_w, const Problem P)
 {
-    using C = swp::Cfg<MP, NS, CH>;
+    using C = swp::Cfg<MP, BPS, NS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     swp::Barriers* bars = reinterpret_cast<swp::Barriers*>(smem + NS * C::kStageBytes);
@@ -1431,7 +1437,8 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
     const int num_tiles = P.tiles_n;  // tiles of 128 columns of y (rows of W)
     const int my_tiles =
         static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
-    const int total = my_tiles * P.nk;
+    const int spt = (P.nk + BPS - 1) / BPS;  // stages per tile; the last may hold fewer blocks
+    const int total = my_tiles * spt;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -1451,7 +1458,7 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
         tma_prefetch_desc(&tmap_w);
     }
     if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, swp::kTmemCols);
+        tmem_alloc(&bars->tmem_base, C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -1460,23 +1467,28 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer: the W tile and the x rows of both planes per K block ----------------
+        // ---------------- TMA producer: per stage, BPS K blocks of the W tile and of both planes ----------------
         int issued = 0;
         grid_dependency_wait();  // the planes come from the previous kernel of the stream
-        int t = static_cast<int>(blockIdx.x), kb = 0;
+        int t = static_cast<int>(blockIdx.x), sk = 0;
         for (int g = 0; g < total; ++g) {
             const int s = g % NS;
             if (g >= NS && !wait_bounded(&bars->empty[s], ((g / NS) - 1) & 1, &bars->abort, kFaultSwpProducer))
                 break;
+            const int kb0 = sk * BPS;
+            const int n = P.nk - kb0 < BPS ? P.nk - kb0 : BPS;
             uint8_t* st = smem + s * C::kStageBytes;
-            const int k0 = kb * BK;
-            mbar_arrive_expect_tx(&bars->full[s], C::kStageBytes);
-            tma_load_2d(st, &tmap_w, &bars->full[s], k0, t * swp::kTileN);
-            tma_load_2d(st + C::kWBytes, &tmap_hi, &bars->full[s], k0, 0);              // rows >= M read as 0
-            tma_load_2d(st + C::kWBytes + C::kXBox, &tmap_lo, &bars->full[s], k0, 0);
+            mbar_arrive_expect_tx(&bars->full[s], n * (C::kWBox + 2 * C::kXBox));
+            for (int i = 0; i < n; ++i)
+                tma_load_2d(st + i * C::kWBox, &tmap_w, &bars->full[s], (kb0 + i) * BK, t * swp::kTileN);
+            for (int i = 0; i < n; ++i) {  // rows >= M read as 0
+                uint8_t* xb = st + BPS * C::kWBox + i * 2 * C::kXBox;
+                tma_load_2d(xb, &tmap_hi, &bars->full[s], (kb0 + i) * BK, 0);
+                tma_load_2d(xb + C::kXBox, &tmap_lo, &bars->full[s], (kb0 + i) * BK, 0);
+            }
             issued = g + 1;
-            if (++kb == P.nk) {
-                kb = 0;
+            if (++sk == spt) {
+                sk = 0;
                 t += static_cast<int>(gridDim.x);
             }
         }
@@ -1484,57 +1496,39 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
                 drain_wait(&bars->full[g % NS], (g / NS) & 1);
     } else if (warp == 1) {
-        // ---------------- MMA issuer, one chunk of CH K blocks at a time ----------------
-        // The whole warp runs the loop (warp-uniform descriptors); lane 0 issues.
-        // What chunk (g, c) of n blocks needs: its stages, and from the third
-        // chunk on its accumulator buffer back from promotion; tested ahead,
-        // waited for only when still pending.
+        // ---------------- MMA issuer, one stage (= one accumulation chunk) at a time ----------------
+        // The whole warp runs the loop (warp-uniform descriptors); lane 0 waits and issues.
         const uint32_t leader = lane == 0 ? 1u : 0u;
         const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
-        auto test_chunk = [&](int g, int c, int n) -> bool {
-            bool r = c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1);
-            for (int i = 0; i < n; ++i)
-                r = mbar_test_wait(&bars->full[(g + i) % NS], ((g + i) / NS) & 1) && r;
-            return r;
-        };
-        auto wait_chunk = [&](int g, int c, int n) -> bool {
-            bool ok = true;
+        int sk = 0;
+        bool ok = true;
+        for (int g = 0; g < total; ++g) {
+            const int s = g % NS, b = g & 1;
+            const int n = P.nk - sk * BPS < BPS ? P.nk - sk * BPS : BPS;
+            // the stage's data, and from the third stage on its accumulator buffer back from promotion
+            bool r = true;
             if (lane == 0) {
-                for (int i = 0; i < n && ok; ++i)
-                    ok = wait_bounded(&bars->full[(g + i) % NS], ((g + i) / NS) & 1, &bars->abort, kFaultSwpMma);
-                if (ok && c >= 2)
-                    ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort, kFaultSwpMma);
+                r = wait_bounded(&bars->full[s], (g / NS) & 1, &bars->abort, kFaultSwpMma);
+                if (r && g >= 2)
+                    r = wait_bounded(&bars->dfree[b], ((g >> 1) - 1) & 1, &bars->abort, kFaultSwpMma);
             }
-            return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        };
-        int g = 0, c = 0, kb = 0;
-        int n = (P.nk < CH) ? P.nk : CH;
-        bool ok = total == 0 || wait_chunk(0, 0, n);
-        while (g < total && ok) {
-            const int b = c & 1;
+            ok = __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+            if (!ok)
+                break;
             tc_fence_after();
             const uint32_t d = tmem + b * C::kCols;
-            const int g2 = g + n, c2 = c + 1;
-            const int kb2 = (kb + n == P.nk) ? 0 : kb + n;
-            const int n2 = (P.nk - kb2 < CH) ? P.nk - kb2 : CH;
-            bool ready2 = true;
+            const uint64_t st = desc0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
             for (int i = 0; i < n; ++i) {
-                const uint64_t st = desc0 + static_cast<uint64_t>((((g + i) % NS) * C::kStageBytes) >> 4);
-                const uint64_t a = st, bx = st + (C::kWBytes >> 4);  // A: W tile; B: hi rows then lo rows
-                if (i == n - 1 && g2 < total)
-                    ready2 = test_chunk(g2, c2, n2);
+                const uint64_t a = st + static_cast<uint64_t>((i * C::kWBox) >> 4);  // A: W tile
+                const uint64_t bx = st + static_cast<uint64_t>((BPS * C::kWBox + i * 2 * C::kXBox) >> 4);  // B: hi, lo
 #pragma unroll
                 for (int j = 0; j < BK / 16; ++j)
                     umma_f16_by(leader, d, a + 2 * j, bx + 2 * j, C::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
-                umma_commit_by(leader, &bars->empty[(g + i) % NS]);
             }
+            umma_commit_by(leader, &bars->empty[s]);
             umma_commit_by(leader, &bars->dfull[b]);
-            g = g2;
-            c = c2;
-            kb = kb2;
-            n = n2;
-            if (g < total && !ready2)
-                ok = wait_chunk(g, c, n);
+            if (++sk == spt)
+                sk = 0;
         }
         if (!ok) {
             umma_commit_by(leader, &bars->drain);
@@ -1551,13 +1545,12 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             Rh[i] = 0.0f;
             Rl[i] = 0.0f;
         }
-        int g = 0, c = 0, kb = 0;
+        int sk = 0;
         int t = static_cast<int>(blockIdx.x);
-        while (g < total) {
-            const int n = (P.nk - kb < CH) ? P.nk - kb : CH;
-            const int b = c & 1;
+        for (int g = 0; g < total; ++g) {
+            const int b = g & 1;
             if (warp == 4)
-                (void)lane0_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultSwpPromote);
+                (void)lane0_wait(&bars->dfull[b], (g >> 1) & 1, &bars->abort, kFaultSwpPromote);
             asm volatile("bar.sync 1, %0;" ::"n"(32 * swp::kPromoters) : "memory");
             if (*reinterpret_cast<volatile int*>(&bars->abort))
                 break;
@@ -1577,10 +1570,7 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
                 Rh[i] = __fadd_rn(Rh[i], __uint_as_float(v[i]));
                 Rl[i] = __fadd_rn(Rl[i], __uint_as_float(v[MP + i]));
             }
-            g += n;
-            ++c;
-            kb += n;
-            if (kb == P.nk) {
+            if (++sk == spt) {
                 // tile finished: this thread holds column col of y for rows 0..M-1
                 const int64_t col = static_cast<int64_t>(t) * swp::kTileN + wq * 32 + lane;
                 if (col < P.N) {
@@ -1594,7 +1584,7 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
                     Rh[i] = 0.0f;
                     Rl[i] = 0.0f;
                 }
-                kb = 0;
+                sk = 0;
                 t += static_cast<int>(gridDim.x);
             }
         }
@@ -1604,7 +1594,7 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, swp::kTmemCols);
+        tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
@@ -1815,11 +1805,11 @@ comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, con
                       P);
 }
 
-template <int MP, int NS, int CH>
+template <int MP, int BPS, int NS>
 comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                           const DeviceInfo& dev, cudaStream_t stream)
 {
-    using C = swp::Cfg<MP, NS, CH>;
+    using C = swp::Cfg<MP, BPS, NS>;
     static std::mutex mu;
     static bool done[64] = {};
     {
@@ -1827,7 +1817,7 @@ comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CU
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (!done[dev.device]) {
-            if (cudaFuncSetAttribute(comp_f16x2_swap_kernel<MP, NS, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(comp_f16x2_swap_kernel<MP, BPS, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(C::kSmem)) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return COMP_ERR_CUDA;
@@ -1836,7 +1826,7 @@ comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CU
         }
     }
     const int grid = P.tiles_n < dev.sm_count ? P.tiles_n : dev.sm_count;
-    return launch_pdl(comp_f16x2_swap_kernel<MP, NS, CH>, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
+    return launch_pdl(comp_f16x2_swap_kernel<MP, BPS, NS>, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
 }
 
 template <int BN, int NS, int CH, int AR = BM>
@@ -1991,8 +1981,10 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
             !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, mp) ||
             !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(swp::kTileN)))
             return COMP_ERR_CUDA;
-        return mp == 16 ? launch_swap<16, 8, 4>(th, tl, tw, P, dev, stream)
-                        : launch_swap<32, 8, 4>(th, tl, tw, P, dev, stream);
+        // three K blocks per stage, three stages: of 1..5 blocks per stage, the
+        // fastest stream of W on GB300 (4.1 TB/s at 16 x 14336 x 4096)
+        return mp == 16 ? launch_swap<16, 3, 3>(th, tl, tw, P, dev, stream)
+                        : launch_swap<32, 3, 3>(th, tl, tw, P, dev, stream);
     }
     if (pairs) {
         // CTA pairs on 256-row tiles
