@@ -139,7 +139,11 @@ comp_status_t comp_merge_f32(const float* acc_hi, const float* acc_lo, float* y,
 comp_status_t comp_gemm_f32x16_variant(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                        int variant, comp_stream_t stream)
 {
-    if (variant < 0 || variant > 2)
+    if (variant < 0 || variant > 3)
+        return COMP_ERR_INVALID_VALUE;
+    // the fused swapped-operand kernel: at most 32 rows, TMA-legal W and x
+    if (variant == 3 && (M > 32 || K % 8 != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0 ||
+                         (reinterpret_cast<uintptr_t>(W) & 15u) != 0))
         return COMP_ERR_INVALID_VALUE;
     DeviceInfo dev;
     bool empty;
@@ -228,6 +232,10 @@ comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, i
         (overlap(workspace, workspace_bytes, x, 4 * M * K) || overlap(workspace, workspace_bytes, W, 2 * N * K) ||
          overlap(workspace, workspace_bytes, y, 4 * M * N)))
         return COMP_ERR_INVALID_VALUE;
+    // at most 32 rows against a wide W: one kernel with the split fused needs
+    // no workspace and is faster than the two-pass form
+    if (swap_fused_preferred(x, W, M, N, K))
+        return launch_swap_fused(x, W, y, M, N, K, dev, s);
     uint16_t* const ws = static_cast<uint16_t*>(workspace);
     const bool ws_aligned = (reinterpret_cast<uintptr_t>(workspace) & 15u) == 0;
     // two-pass form on the caller's W: planes [M, K] in the workspace

@@ -1383,6 +1383,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
 // buffers and promotion adds both halves into FP32 registers.  The epilogue
 // merges y = R_hi + rn(2^-10 R_lo); a warp stores 32 consecutive columns of
 // one row of y per instruction.
+//
+// FX (fused split): the kernel reads FP32 x instead of the planes.  The
+// producer loads the stage's FP32 x boxes (L2-resident: every CTA reads all of
+// x) into a staging area of the stage by TMA, with their own barrier, at the
+// same time as the W boxes, so their latency hides behind that of W.  Two
+// warps then split the staged values with the arithmetic of comp_split_f32
+// and store hi and lo where the planes' TMA boxes would have put them.  TMA
+// fills rows >= M and columns >= K with zeros, so the split needs no bounds.
+// One kernel then does the whole projection, with no planes in HBM.
 // ---------------------------------------------------------------------------
 namespace swp {
 constexpr int kPromoters = 4;
@@ -1390,13 +1399,15 @@ constexpr int kThreads = 128 + 32 * kPromoters;  // warpgroup 0: producer, MMA i
 constexpr int kTileN = 128;                       // W rows per tile (the MMA's M)
 constexpr int kMaxStages = 8;
 
-template <int MP, int BPS, int NS>
+template <int MP, int BPS, int NS, bool FX>
 struct Cfg {
     static_assert(MP == 16 || MP == 32, "padded rows of x");
     static_assert(BPS >= 1 && BPS <= 8 && NS >= 2 && NS <= kMaxStages, "pipeline");
     static constexpr uint32_t kWBox = kTileN * BK * 2;  // 16 KB: one K block of the W tile
     static constexpr uint32_t kXBox = MP * BK * 2;      // one plane's Mp rows of one K block
-    static constexpr uint32_t kStageBytes = BPS * (kWBox + 2 * kXBox);
+    static constexpr uint32_t kXF = MP * BK * 4;        // FX: the FP32 x rows of one K block
+    static constexpr uint32_t kXFOff = BPS * (kWBox + 2 * kXBox);
+    static constexpr uint32_t kStageBytes = kXFOff + (FX ? BPS * kXF : 0u);
     static_assert(kXBox % 1024 == 0, "128-byte swizzle atoms");
     static constexpr size_t kSmem = 1024 + NS * kStageBytes + 512;
     static_assert(kSmem <= 232448, "shared memory");
@@ -1408,6 +1419,7 @@ struct Cfg {
 struct Barriers {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
+    uint64_t xfull[kMaxStages];  // FX: the FP32 x boxes of the stage landed
     uint64_t dfull[2];
     uint64_t dfree[2];
     uint64_t drain;
@@ -1420,13 +1432,15 @@ struct Barriers {
 constexpr uint32_t kFaultSwpProducer = 0x801;
 constexpr uint32_t kFaultSwpMma = 0x802;
 constexpr uint32_t kFaultSwpPromote = 0x803;
+constexpr uint32_t kFaultSwpSplit = 0x804;
 
-template <int MP, int BPS, int NS>
+// FX: tmap_hi is the map of FP32 x (boxes of 64 x Mp, no swizzle); tmap_lo is unused.
+template <int MP, int BPS, int NS, bool FX>
 __global__ void __launch_bounds__(swp::kThreads, 1)
     comp_f16x2_swap_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
                            const __grid_constant__ CUtensorMap tmap_w, const Problem P)
 {
-    using C = swp::Cfg<MP, BPS, NS>;
+    using C = swp::Cfg<MP, BPS, NS, FX>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     swp::Barriers* bars = reinterpret_cast<swp::Barriers*>(smem + NS * C::kStageBytes);
@@ -1442,8 +1456,9 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->full[s], FX ? 3 : 1);  // FX: the W bytes and both split warps
             mbar_init(&bars->empty[s], 1);
+            mbar_init(&bars->xfull[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars->dfull[b], 1);
@@ -1454,7 +1469,8 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
         fence_mbar_init();
         fence_proxy_async_smem();
         tma_prefetch_desc(&tmap_hi);
-        tma_prefetch_desc(&tmap_lo);
+        if (!FX)
+            tma_prefetch_desc(&tmap_lo);
         tma_prefetch_desc(&tmap_w);
     }
     if (warp == 1) {
@@ -1478,10 +1494,15 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             const int kb0 = sk * BPS;
             const int n = P.nk - kb0 < BPS ? P.nk - kb0 : BPS;
             uint8_t* st = smem + s * C::kStageBytes;
-            mbar_arrive_expect_tx(&bars->full[s], n * (C::kWBox + 2 * C::kXBox));
+            if (FX) {  // the FP32 x rows first: the split warps need them before the MMA needs W
+                mbar_arrive_expect_tx(&bars->xfull[s], n * C::kXF);
+                for (int i = 0; i < n; ++i)
+                    tma_load_2d(st + C::kXFOff + i * C::kXF, &tmap_hi, &bars->xfull[s], (kb0 + i) * BK, 0);
+            }
+            mbar_arrive_expect_tx(&bars->full[s], n * (C::kWBox + (FX ? 0u : 2 * C::kXBox)));
             for (int i = 0; i < n; ++i)
                 tma_load_2d(st + i * C::kWBox, &tmap_w, &bars->full[s], (kb0 + i) * BK, t * swp::kTileN);
-            for (int i = 0; i < n; ++i) {  // rows >= M read as 0
+            for (int i = 0; i < n && !FX; ++i) {  // rows >= M read as 0
                 uint8_t* xb = st + BPS * C::kWBox + i * 2 * C::kXBox;
                 tma_load_2d(xb, &tmap_hi, &bars->full[s], (kb0 + i) * BK, 0);
                 tma_load_2d(xb + C::kXBox, &tmap_lo, &bars->full[s], (kb0 + i) * BK, 0);
@@ -1493,8 +1514,11 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             }
         }
         if (*reinterpret_cast<volatile int*>(&bars->abort))
-            for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
+            for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g) {
+                if (FX)
+                    drain_wait(&bars->xfull[g % NS], (g / NS) & 1);
                 drain_wait(&bars->full[g % NS], (g / NS) & 1);
+            }
     } else if (warp == 1) {
         // ---------------- MMA issuer, one stage (= one accumulation chunk) at a time ----------------
         // The whole warp runs the loop (warp-uniform descriptors); lane 0 waits and issues.
@@ -1535,6 +1559,46 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             if (lane == 0)
                 drain_wait(&bars->drain, 0);
             __syncwarp();
+        }
+    } else if (FX && (warp == 2 || warp == 3)) {
+        // ---------------- split: staged FP32 x of each stage -> hi and lo in the stage ----------------
+        // Item (block i, row m, 16-byte chunk c): 8 consecutive x of row m,
+        // stored where a 128-byte-swizzled TMA box of the planes would put them.
+        constexpr int kItems = BPS * MP * 8;
+        constexpr int kPer = (kItems + 63) / 64;
+        const int lt = static_cast<int>(threadIdx.x) - 64;
+        int sk = 0;
+        for (int g = 0; g < total; ++g) {
+            const int s = g % NS;
+            if (!warp_wait(&bars->xfull[s], (g / NS) & 1, &bars->abort, kFaultSwpSplit))
+                break;
+            const int n = P.nk - sk * BPS < BPS ? P.nk - sk * BPS : BPS;
+            uint8_t* st = smem + s * C::kStageBytes;
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int it = lt + 64 * u;
+                const int i = it / (MP * 8), m = (it / 8) % MP, c = it % 8;
+                if (it < kItems && i < n) {
+                    const float4* src = reinterpret_cast<const float4*>(st + C::kXFOff + i * C::kXF + m * (BK * 4) + c * 32);
+                    const float4 va = src[0], vb = src[1];
+                    uint32_t h[4], l[4];
+                    split2(va.x, va.y, h[0], l[0]);
+                    split2(va.z, va.w, h[1], l[1]);
+                    split2(vb.x, vb.y, h[2], l[2]);
+                    split2(vb.z, vb.w, h[3], l[3]);
+                    uint8_t* hb = st + BPS * C::kWBox + i * 2 * C::kXBox + m * 128 + ((c ^ (m & 7)) << 4);
+                    st_shared_v4(hb, __uint_as_float(h[0]), __uint_as_float(h[1]), __uint_as_float(h[2]),
+                                 __uint_as_float(h[3]));
+                    st_shared_v4(hb + C::kXBox, __uint_as_float(l[0]), __uint_as_float(l[1]), __uint_as_float(l[2]),
+                                 __uint_as_float(l[3]));
+                }
+            }
+            fence_proxy_async_smem();  // generic-proxy stores, read next by the tensor cores
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->full[s]);
+            if (++sk == spt)
+                sk = 0;
         }
     } else if (warp >= 4) {
         // ---------------- promotion and epilogue (lane quarter wq = rows 32 wq .. of the tile) ----------------
@@ -1708,6 +1772,13 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
                              int variant, const DeviceInfo& dev, cudaStream_t stream)
 {
     const bool vec_ok = aligned16(x) && aligned16(W) && (K % 8 == 0);
+    // at most 32 rows: the swapped-operand kernel with the split fused (variant
+    // 3, or automatically once W spans at least 32 tiles of 128 rows)
+    if (variant == 3 || (variant == 0 && swap_fused_preferred(x, W, M, N, K))) {
+        if (!vec_ok || M > 32)
+            return COMP_ERR_INVALID_VALUE;
+        return launch_swap_fused(x, W, y, M, N, K, dev, stream);
+    }
     if (variant == 1 && !vec_ok)
         return COMP_ERR_INVALID_VALUE;
     bool use_vec = variant == 2 ? false : vec_ok;
@@ -1805,11 +1876,11 @@ comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, con
                       P);
 }
 
-template <int MP, int BPS, int NS>
+template <int MP, int BPS, int NS, bool FX = false>
 comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                           const DeviceInfo& dev, cudaStream_t stream)
 {
-    using C = swp::Cfg<MP, BPS, NS>;
+    using C = swp::Cfg<MP, BPS, NS, FX>;
     static std::mutex mu;
     static bool done[64] = {};
     {
@@ -1817,7 +1888,7 @@ comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CU
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (!done[dev.device]) {
-            if (cudaFuncSetAttribute(comp_f16x2_swap_kernel<MP, BPS, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(comp_f16x2_swap_kernel<MP, BPS, NS, FX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(C::kSmem)) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return COMP_ERR_CUDA;
@@ -1826,7 +1897,7 @@ comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CU
         }
     }
     const int grid = P.tiles_n < dev.sm_count ? P.tiles_n : dev.sm_count;
-    return launch_pdl(comp_f16x2_swap_kernel<MP, BPS, NS>, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
+    return launch_pdl(comp_f16x2_swap_kernel<MP, BPS, NS, FX>, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
 }
 
 template <int BN, int NS, int CH, int AR = BM>
@@ -1981,10 +2052,12 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
             !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, mp) ||
             !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(swp::kTileN)))
             return COMP_ERR_CUDA;
-        // three K blocks per stage, three stages: of 1..5 blocks per stage, the
-        // fastest stream of W on GB300 (4.1 TB/s at 16 x 14336 x 4096)
-        return mp == 16 ? launch_swap<16, 3, 3>(th, tl, tw, P, dev, stream)
-                        : launch_swap<32, 3, 3>(th, tl, tw, P, dev, stream);
+        // two K blocks per stage: with 2 or 3 per stage W streams at 4.1 TB/s
+        // on GB300 at 16 x 14336 x 4096 (one per stage: 3.0-3.8).  The fused
+        // kernel has the same stages (fewer of them, for its FP32 staging),
+        // hence the same chunks: both forms give identical bits.
+        return mp == 16 ? launch_swap<16, 2, 5>(th, tl, tw, P, dev, stream)
+                        : launch_swap<32, 2, 4>(th, tl, tw, P, dev, stream);
     }
     if (pairs) {
         // CTA pairs on 256-row tiles
@@ -2041,6 +2114,41 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     if (bn == 128)
         return launch_x2_bn<128, 4, 2>(th, tl, tw, P, dev, stream);
     return launch_x2_bn<96, 4, 2>(th, tl, tw, P, dev, stream);
+}
+
+bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K)
+{
+    return M <= 32 && (N + swp::kTileN - 1) / swp::kTileN >= 32 && K % 8 == 0 && aligned16(x) && aligned16(W);
+}
+
+comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                                const DeviceInfo& dev, cudaStream_t stream)
+{
+    if (M > 32 || K % 8 != 0 || !aligned16(x) || !aligned16(W))
+        return COMP_ERR_INVALID_VALUE;
+    Problem P;
+    P.x = x;
+    P.W = W;
+    P.y = y;
+    P.M = static_cast<int>(M);
+    P.N = static_cast<int>(N);
+    P.K = static_cast<int>(K);
+    P.nk = static_cast<int>((K + BK - 1) / BK);
+    P.vec_y = (N % 4 == 0) && aligned16(y);
+    P.tma_y = 0;
+    P.tiles_m = 1;
+    P.tiles_n = static_cast<int>((N + swp::kTileN - 1) / swp::kTileN);
+    if (static_cast<int64_t>(P.tiles_n) * P.nk > INT32_MAX / 2)
+        return COMP_ERR_INVALID_VALUE;
+    const uint32_t mp = M <= 16 ? 16u : 32u;
+    CUtensorMap tx{}, tw{}, none{};  // FP32 x in the first map's place; the second is not read
+    if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, K, M, BK, mp, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(swp::kTileN)))
+        return COMP_ERR_CUDA;
+    // two K blocks per stage as in the two-pass kernel; the FP32 staging makes
+    // a stage larger: 4 x 48 KB (Mp 16), 3 x 64 KB (Mp 32)
+    return mp == 16 ? launch_swap<16, 2, 4, true>(tx, none, tw, P, dev, stream)
+                    : launch_swap<32, 2, 3, true>(tx, none, tw, P, dev, stream);
 }
 
 namespace {

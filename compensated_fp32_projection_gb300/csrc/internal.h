@@ -31,6 +31,11 @@ comp_status_t launch_merge(const float* acc_hi, const float* acc_lo, float* y, i
 comp_status_t launch_gemm_simt(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                const DeviceInfo& dev, cudaStream_t stream);
 // variant: 0 automatic, 1 TMA loads, 2 plain loads.
+// Fused split and swapped-operand product for at most 32 rows of x (K a
+// multiple of 8, x and W 16-byte aligned); preferred once N spans 32 tiles of 128.
+bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K);
+comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                                const DeviceInfo& dev, cudaStream_t stream);
 comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                              int variant, const DeviceInfo& dev, cudaStream_t stream);
 

@@ -94,7 +94,10 @@ comp_status_t comp_merge_f32(const float* acc_hi, const float* acc_lo, float* y,
  *   tensor-core accumulations of hi(x)·W^T and lo(x)·W^T.
  *   x : [M, K] binary32 (input).   W : [N, K] binary16 (input).   y : [M, N] binary32 (output).
  * One kernel: x is split on the fly in shared memory, both products accumulate
- * in tensor memory, and the merge is the epilogue.  The accumulation order of
+ * in tensor memory, and the merge is the epilogue.  For at most 32 rows
+ * against at least 32 * 128 rows of W (K a multiple of 8, x and W 16-byte
+ * aligned) the kernel swaps the operands (y^T = W x^T, 128 rows of W per MMA)
+ * and splits each K block of x into shared memory as it streams W.  The accumulation order of
  * the tensor cores is not specified; results agree with an FP64 evaluation of
  * the same formula to within 4e-6 * sum_k |x[m,k]| |W[n,k]| per element.
  * Errors: COMP_ERR_INVALID_VALUE if a size is negative, M*K, N*K or M*N
@@ -119,7 +122,10 @@ comp_status_t comp_gemm_f32_simt(const float* x, const uint16_t* W, float* y, in
  *   0 = automatic (what comp_gemm_f32x16 does),
  *   1 = tiled tensor-memory-accelerator loads of x and W (needs 16-byte aligned
  *       x and W and K % 8 == 0, else COMP_ERR_INVALID_VALUE),
- *   2 = plain coalesced loads (any alignment and size).
+ *   2 = plain coalesced loads (any alignment and size),
+ *   3 = the swapped-operand kernel with the split fused (M <= 32, 16-byte
+ *       aligned x and W, K % 8 == 0, else COMP_ERR_INVALID_VALUE).
+ * A variant outside 0..3 is COMP_ERR_INVALID_VALUE.
  */
 comp_status_t comp_gemm_f32x16_variant(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N,
                                        int64_t K, int variant, comp_stream_t stream);
@@ -177,6 +183,9 @@ int64_t comp_gemm_workspace_bytes_mnk(int64_t M, int64_t N, int64_t K);
  * (COMP_ERR_INVALID_VALUE); its contents are overwritten.  The call enqueues
  * the two-pass form: comp_split_f32 of x into the workspace, then
  * comp_gemm_f16x2.
+ *   - M <= 32 against at least 32 * 128 rows of W, K a multiple of 8, x and W
+ *     16-byte aligned: the fused swapped-operand kernel of comp_gemm_f32x16
+ *     instead (faster there than split plus product); the workspace is unused.
  *   - K a multiple of 8, W 16-byte aligned, workspace of at least
  *     comp_gemm_workspace_bytes(M, K): the planes [M, K] (hi, then lo) and
  *     the caller's W.

@@ -82,6 +82,11 @@ def test_gemm_argument_errors(lib):
         assert fn(P(4096), P(1 << 20), P(1 << 24), 1 << 31, 4, 4, None) == 1  # M beyond int32
         assert fn(None, None, None, 0, 5, 7, None) == 0  # empty output: no-op
     assert lib.comp_gemm_f32x16_variant(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, 7, None) == 1
+    # variant 3 (split fused into the swapped-operand kernel): M <= 32, K % 8 == 0, aligned x and W
+    assert lib.comp_gemm_f32x16_variant(P(4096), P(1 << 20), P(1 << 24), 33, 4096, 64, 3, None) == 1
+    assert lib.comp_gemm_f32x16_variant(P(4096), P(1 << 20), P(1 << 24), 16, 4096, 60, 3, None) == 1
+    assert lib.comp_gemm_f32x16_variant(P(4096 + 4), P(1 << 20), P(1 << 24), 16, 4096, 64, 3, None) == 1
+    assert lib.comp_gemm_f32x16_variant(P(4096), P((1 << 20) + 2), P(1 << 24), 16, 4096, 64, 3, None) == 1
 
 
 def test_two_pass_argument_errors(lib):

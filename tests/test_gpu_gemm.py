@@ -193,3 +193,63 @@ def test_simt_true_fp32(pkg, orc, shape):
 def test_device_status_clean_after_gemms(pkg):
     st, where = pkg.device_status()
     assert st == 0 and where == 0
+
+
+# At most 32 rows: the split fused into the swapped-operand kernel (automatic
+# once W spans 32 tiles of 128 rows; variant 3 forces it).  Ragged N tails,
+# K below one 64-wide block, K not a multiple of 64, one and 32 rows.
+SWAPPED = [(16, 14336, 4096), (1, 4096, 64), (17, 5000, 520), (32, 4100, 1032), (5, 4096, 8), (32, 8192, 200),
+           (8, 384, 256), (3, 130, 72)]
+
+
+@pytest.mark.parametrize("shape", SWAPPED, ids=lambda s: "x".join(map(str, s)))
+def test_fused_swapped(pkg, orc, shape):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=M * 13 + N + K, scale=2.0)
+    y = pkg.comp_gemm_f32x16_variant(x.cuda(), W.cuda(), 3)
+    e_gpu, e_cast = check_comp(y, x, W, orc)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+    if (N + 127) // 128 >= 32:  # the automatic choice is the same kernel
+        y0 = pkg.comp_gemm_f32x16(x.cuda(), W.cuda())
+        assert torch.equal(y0.view(torch.int32), y.view(torch.int32))
+
+
+@pytest.mark.parametrize("shape", [(16, 14336, 4096), (32, 4100, 1032), (7, 2048, 136)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_fused_split_equals_standalone_split(pkg, shape):
+    # the in-kernel split is the arithmetic of comp_split_f32 and the stages
+    # and chunks are those of the two-pass swapped kernel: bit-identical y
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=N + K, scale=3.0)
+    x, W = x.cuda(), W.cuda()
+    hi, lo = pkg.comp_split_f32(x)
+    y2 = pkg.comp_gemm_f16x2_variant(hi, lo, W, 3)
+    y1 = pkg.comp_gemm_f32x16_variant(x, W, 3)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+
+
+def test_fused_swapped_special_values(pkg, orc):
+    # the tiny workload's hand-set x values (exact FP16 values, halfway ties,
+    # subnormals, +-60000) through the in-kernel split
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs("tiny")
+    y = pkg.comp_gemm_f32x16_variant(x.cuda(), W.cuda(), 3)
+    e_gpu, e_cast = check_comp(y, x, W, orc)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+
+
+def test_fused_swapped_rejects(pkg):
+    from compensated_fp32_projection_gb300 import CompError
+
+    W = torch.zeros(4096, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(CompError):
+        pkg.comp_gemm_f32x16_variant(torch.zeros(33, 64, device="cuda"), W, 3)
+    with pytest.raises(CompError):  # K % 8 != 0
+        pkg.comp_gemm_f32x16_variant(torch.zeros(4, 60, device="cuda"), torch.zeros(4096, 60, dtype=torch.float16,
+                                                                                   device="cuda"), 3)
+
