@@ -65,6 +65,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value, dist, device):
+    """The slowest rank's time (every rank receives it); value itself on one rank."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, work_per_rank, seconds):
+    """Whole-job rate: the work of all ranks (replicas, fixed work per rank) over
+    the slowest rank's time."""
+    return world * work_per_rank / seconds
+
+
 def load_peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -352,17 +369,13 @@ def run_ours(args):
     times = [a.elapsed_time(b) for a, _, b in events]  # ms, whole step
     split_times = [a.elapsed_time(m) for a, m, _ in events]
     product_times = [m.elapsed_time(b) for _, m, b in events]
-    ms = statistics.mean(times)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(times), dist, dev)
     st, where = pkg.device_status()
     if st != 0:
         raise RuntimeError(f"kernel fault word {where:#x}")
 
     flops = float(s.flops)
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_throughput(world, flops, ms * 1e-3) / 1e12
 
     # end to end through the public API, pipelined like a serving loop: step i's
     # inputs go up on one copy stream while step i-1 computes and step i-2's
@@ -407,11 +420,7 @@ def run_ours(args):
     run_e2e(e2e_steps)
     b.record(s_out)  # after the last result's copy, which depends on every earlier step
     barrier()
-    e2e_ms = a.elapsed_time(b) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, dist, dev)
 
     peaks, peak_src = load_peaks()
     tensor_flops = 2.0 * flops  # two FP16 products per effective FP32 multiply-add
@@ -519,7 +528,7 @@ def run_ours(args):
             "step_frac_of_roofline": value / world / (peaks["bf16_tflops"] / 2.0),
         },
         "e2e": {
-            "value": world * flops / (e2e_ms * 1e-3) / 1e12,
+            "value": job_throughput(world, flops, e2e_ms * 1e-3) / 1e12,
             "unit": UNIT,
             "h2d_bytes_per_step": 4 * s.M * s.K + 2 * s.N * s.K,
             "d2h_bytes_per_step": 4 * s.M * s.N,
