@@ -143,18 +143,6 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, FP16 inputs, kind::f16.
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar)
@@ -165,20 +153,10 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar)
 
 // ---------------------------------------------------------------------------
 // Warp-wide issue: the whole (converged) warp runs the issuing loop, so that
-// descriptors and addresses are warp-uniform values, and one elected lane
-// executes the tensor-core instruction (a predicate inside the same asm).
+// descriptors and addresses are warp-uniform values, and one chosen lane
+// (`leader` != 0) executes the tensor-core instruction (a predicate inside the
+// same asm).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t elect_one_sync()
-{
-    uint32_t e;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "elect.sync _|p, 0xffffffff;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(e));
-    return e;
-}
-
 __device__ __forceinline__ void umma_f16_by(uint32_t leader, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate)
 {
@@ -212,21 +190,6 @@ __device__ __forceinline__ void umma_commit_by(uint32_t leader, uint64_t* bar)
         "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
         "r"(leader)
         : "memory");
-}
-
-// Warp-wide: 32 TMEM lanes x 32 consecutive 32-bit columns; thread i receives
-// lane (base lane + i), columns [col, col + 32).
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld_wait()
@@ -418,12 +381,6 @@ __device__ __forceinline__ void grid_dependency_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
-
-__device__ __forceinline__ void grid_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 
 // ---------------------------------------------------------------------------
 // Exchanges of generic data between the CTAs of a cluster (distributed shared
