@@ -57,6 +57,9 @@ def _load():
         lib.oracle_default_threads.restype = c_int
         lib.oracle_split.argtypes = [vp, vp, vp, i64, c_int]
         lib.oracle_merge.argtypes = [vp, vp, vp, i64, c_int]
+        lib.oracle_epilogue.argtypes = [vp, vp, vp, vp, i64, i64, c_int]
+        lib.oracle_gelu.argtypes = [ctypes.c_double]
+        lib.oracle_gelu.restype = ctypes.c_double
         for name in ("oracle_gemm_comp", "oracle_gemm_true", "oracle_gemm_cast", "oracle_gemm_den"):
             getattr(lib, name).argtypes = [vp, vp, i64, i64, i64, vp, vp, i64, vp, c_int]
         _lib = lib
@@ -143,3 +146,28 @@ def gemm_cast(x, W, rows=None, cols=None, threads: int = 0) -> np.ndarray:
 def gemm_den(x, W, rows=None, cols=None, threads: int = 0) -> np.ndarray:
     """Error scale per output: sum |x|*|w| (float64)."""
     return _gemm("oracle_gemm_den", x, W, rows, cols, threads, np.float64)
+
+
+def gelu(g: float) -> float:
+    """The exact GELU g * Phi(g) in double."""
+    return float(_load().oracle_gelu(float(g)))
+
+
+def epilogue(y, bias=None, gate=None, threads: int = 0) -> np.ndarray:
+    """out = gelu(gate) * (y + bias) per element of y [M, N], bias [N] and gate
+    [M, N] optional; double arithmetic, rounded once to binary32."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    if y.ndim != 2:
+        raise ValueError("y must be [M, N]")
+    M, N = y.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    g = None if gate is None else np.ascontiguousarray(gate, dtype=np.float32)
+    if b is not None and b.shape != (N,):
+        raise ValueError("bias must be [N]")
+    if g is not None and g.shape != (M, N):
+        raise ValueError("gate must be [M, N]")
+    out = np.empty((M, N), np.float32)
+    _load().oracle_epilogue(_ptr(y), None if b is None else _ptr(b), None if g is None else _ptr(g), _ptr(out), M, N,
+                            threads)
+    return out
+

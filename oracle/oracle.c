@@ -16,6 +16,10 @@
  *     cannot overflow binary16 for large activations).
  * The merge formula y = acc_hi + acc_lo * 2^-10 is the plain reading of the
  * FP32 combination with the 1024 scale undone.
+ *   - feed-forward paragraph: the FP32 feed-forward layers fuse the GEGLU gate
+ *     activation and multiplication into one dispatch.  oracle_epilogue is that
+ *     step on a projection's output, read as out = gelu(gate) * (y + bias) with
+ *     the exact GELU, g * Phi(g), Phi the standard normal distribution function.
  *
  * Every floating-point step here is done in IEEE double, where each step used is
  * exact, and then rounded once to the target format.  Compile with
@@ -416,3 +420,51 @@ void oracle_gemm_den(const float* x, const uint16_t* W, int64_t M, int64_t N, in
 {
     gemm_run(GEMM_DEN, x, W, M, N, K, rows, cols, count, NULL, den, nthreads);
 }
+
+/* ------------------------------------------------------------------------- */
+/* Epilogue of a GEGLU feed-forward step on a projection's output y [M, N]:   */
+/*   out[m, n] = gelu(gate[m, n]) * (y[m, n] + bias[n]),                     */
+/*   gelu(g) = g * Phi(g),  Phi(g) = erfc(-g / sqrt(2)) / 2,                 */
+/* (the same function as (1 + erf(g / sqrt 2)) / 2, without its cancellation  */
+/* for negative g),                                                          */
+/* bias NULL: no bias; gate NULL: factor 1.  Evaluated in double from the     */
+/* binary32 inputs (y + bias is exact in double) and rounded once to binary32. */
+/* ------------------------------------------------------------------------- */
+static double gelu_exact(double g)
+{
+    return 0.5 * g * erfc(-g * 0.70710678118654752440); /* 1/sqrt(2) */
+}
+
+struct epi_ctx {
+    const float* y;
+    const float* bias;
+    const float* gate;
+    float* out;
+    int64_t N;
+};
+
+static void epi_range(int64_t a, int64_t b, void* p)
+{
+    const struct epi_ctx* c = (const struct epi_ctx*)p;
+    for (int64_t i = a; i < b; ++i) {
+        double v = (double)c->y[i];
+        if (c->bias)
+            v += (double)c->bias[i % c->N];
+        if (c->gate)
+            v *= gelu_exact((double)c->gate[i]);
+        c->out[i] = (float)v;
+    }
+}
+
+void oracle_epilogue(const float* y, const float* bias, const float* gate, float* out, int64_t M, int64_t N,
+                     int nthreads)
+{
+    struct epi_ctx c = {y, bias, gate, out, N};
+    parallel_for(M * N, nthreads, epi_range, &c);
+}
+
+double oracle_gelu(double g)
+{
+    return gelu_exact(g);
+}
+
