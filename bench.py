@@ -444,6 +444,15 @@ def run_ours(args):
     fused_tflops = flops / (mean * 1e-3) / 1e12
     med, mean = time_kernel(lambda: pkg.comp_gemm_f32_simt(x, W, y), flush, stream, 3, warm=1)
     simt_tflops = flops / (mean * 1e-3) / 1e12
+    # the GEGLU epilogue (bias and gate) in the product kernel, against the same
+    # two-pass call without it; both through the public calls, same workspace
+    g_ep = torch.Generator(device="cpu").manual_seed(7)
+    b_ep = (torch.randn(s.N, generator=g_ep) * 0.5).to(dev)
+    gate_ep = (torch.randn(s.M, s.N, generator=g_ep) * 2.0).to(dev)
+    med, mean_plain = time_kernel(lambda: pkg.comp_gemm_f32x16_ws(x, W, y, workspace=ws), flush, stream, 20)
+    med, mean_epi = time_kernel(lambda: pkg.comp_gemm_f32x16_epilogue(x, W, b_ep, gate_ep, y, workspace=ws), flush,
+                                stream, 20)
+    del b_ep, gate_ep
     del xs, hi, lo, a32, b32, o32
 
     # the other configurations (parity cases), each through the workspace entry
@@ -545,6 +554,10 @@ def run_ours(args):
             "comp_split_f32": {"n": n, "GB/s": split_gbs, "frac_of_hbm": split_gbs / peaks["hbm_gbs"]},
             "comp_merge_f32": {"n": n, "GB/s": merge_gbs, "frac_of_hbm": merge_gbs / peaks["hbm_gbs"]},
             "comp_gemm_f32_simt": {"TFLOP/s": simt_tflops},
+            "comp_gemm_f32x16_epilogue (bias + GEGLU gate, in the product's epilogue)": {
+                "ms": mean_epi, "eff TFLOP/s": flops / (mean_epi * 1e-3) / 1e12,
+                "ms without the epilogue": mean_plain,
+                "added gate bytes": 4 * s.M * s.N},
         },
         "other_configs": others,
     }

@@ -25,6 +25,8 @@ __all__ = [
     "comp_gemm_f16x2",
     "comp_gemm_f16x2_variant",
     "comp_gemm_f32x16_ws",
+    "comp_gemm_f32x16_epilogue",
+    "comp_gemm_f16x2_epilogue",
     "comp_gemm_workspace_bytes",
     "comp_gemm_workspace_bytes_mnk",
     "comp_gemm_f32x16_noalloc",
@@ -178,6 +180,57 @@ def comp_gemm_f32x16_ws(x, W, y=None, workspace=None, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _native.call("comp_gemm_f32x16_ws", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K, workspace.data_ptr(),
                  nbytes, _stream(x, stream))
+    return y
+
+
+def _epilogue_args(bias, gate, M, N, device):
+    torch = _torch()
+    if bias is not None:
+        _check(bias, torch.float32, "bias")
+        if tuple(bias.shape) != (N,) or bias.device != device:
+            raise ValueError("bias must be a [N] float32 tensor on the output's device")
+    if gate is not None:
+        _check(gate, torch.float32, "gate")
+        if tuple(gate.shape) != (M, N) or gate.device != device:
+            raise ValueError("gate must be a [M, N] float32 tensor on the output's device")
+    return (0 if bias is None else bias.data_ptr()), (0 if gate is None else gate.data_ptr())
+
+
+def comp_gemm_f32x16_epilogue(x, W, bias=None, gate=None, y=None, workspace=None, stream=None):
+    """comp_gemm_f32x16_ws followed, in the product kernel's epilogue, by the
+    GEGLU step y = gelu(gate) * (y + bias) (bias [N] and gate [M, N] float32,
+    each optional; gelu(g) = g * Phi(g))."""
+    torch = _torch()
+    M, N, K, y = _gemm_args(x, W, y)
+    pb, pg = _epilogue_args(bias, gate, M, N, y.device)
+    if workspace is None:
+        aligned = K % 8 == 0 and W.data_ptr() % 16 == 0
+        nbytes = comp_gemm_workspace_bytes(M, K) if aligned else comp_gemm_workspace_bytes_mnk(M, N, K)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    _native.call("comp_gemm_f32x16_epilogue", x.data_ptr(), W.data_ptr(), pb, pg, y.data_ptr(), M, N, K,
+                 workspace.data_ptr(), nbytes, _stream(x, stream))
+    return y
+
+
+def comp_gemm_f16x2_epilogue(hi, lo, W, bias=None, gate=None, variant=0, y=None, stream=None):
+    """comp_gemm_f16x2_variant with the GEGLU epilogue y = gelu(gate) * (y + bias)."""
+    torch = _torch()
+    _check(hi, torch.float16, "hi")
+    _check(lo, torch.float16, "lo")
+    _check(W, torch.float16, "W")
+    if hi.shape != lo.shape or hi.dim() != 2 or W.dim() != 2 or hi.shape[1] != W.shape[1]:
+        raise ValueError("hi and lo must be [M, K] and W [N, K]")
+    M, K = hi.shape
+    N = W.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=hi.device)
+    _check(y, torch.float32, "y")
+    pb, pg = _epilogue_args(bias, gate, M, N, y.device)
+    _native.call("comp_gemm_f16x2_epilogue", hi.data_ptr(), lo.data_ptr(), W.data_ptr(), pb, pg, y.data_ptr(), M, N,
+                 K, int(variant), _stream(hi, stream))
     return y
 
 

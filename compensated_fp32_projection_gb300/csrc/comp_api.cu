@@ -95,6 +95,86 @@ comp_status_t check_gemm(const void* x, int64_t x_elem, const uint16_t* W, float
     return COMP_OK;
 }
 
+// Epilogue operands: bias [N] and gate [M, N] FP32, either may be NULL; neither
+// may overlap y (they are read while y is written).
+bool epilogue_args_ok(const float* bias, const float* gate, const float* y, int64_t M, int64_t N)
+{
+    int64_t mn = 0;
+    if (M < 0 || N < 0 || !mul_ok(M, N, &mn) || mn > INT64_MAX / 4)
+        return false;
+    if (bias && N > 0 && overlap(bias, 4 * N, y, 4 * mn))
+        return false;
+    if (gate && mn > 0 && overlap(gate, 4 * mn, y, 4 * mn))
+        return false;
+    return true;
+}
+
+comp_status_t gemm_ws_impl(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                           void* workspace, int64_t workspace_bytes, comp_stream_t stream, const Epilogue& epi)
+{
+    DeviceInfo dev;
+    bool empty;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const comp_status_t st = check_gemm(x, 4, W, y, M, N, K, s, &dev, &empty);
+    if (st != COMP_OK || empty)
+        return st;
+    if (workspace_bytes < 0 || (workspace_bytes > 0 && !workspace))
+        return COMP_ERR_INVALID_VALUE;
+    if (workspace && workspace_bytes > 0 &&
+        (overlap(workspace, workspace_bytes, x, 4 * M * K) || overlap(workspace, workspace_bytes, W, 2 * N * K) ||
+         overlap(workspace, workspace_bytes, y, 4 * M * N)))
+        return COMP_ERR_INVALID_VALUE;
+    // at most 32 rows against a wide W: one kernel with the split fused needs
+    // no workspace and is faster than the two-pass form
+    if (swap_fused_preferred(x, W, M, N, K))
+        return launch_swap_fused(x, W, y, M, N, K, dev, s, epi);
+    uint16_t* const ws = static_cast<uint16_t*>(workspace);
+    const bool ws_aligned = (reinterpret_cast<uintptr_t>(workspace) & 15u) == 0;
+    // two-pass form on the caller's W: planes [M, K] in the workspace
+    const int64_t need = comp_gemm_workspace_bytes(M, K);
+    if (ws && ws_aligned && need > 0 && workspace_bytes >= need && gemm_f16x2_supported(ws, ws + M * K, W, K)) {
+        const comp_status_t sp = launch_split(x, ws, ws + M * K, M * K, dev, s);
+        if (sp != COMP_OK)
+            return sp;
+        return launch_gemm_f16x2(ws, ws + M * K, W, y, M, N, K, 0, dev, s, epi);
+    }
+    // two-pass form with K padded to a multiple of 8 (any K, any alignment):
+    // planes [M, Kp] and a zero-padded copy of W [N, Kp] in the workspace
+    const int64_t need_p = comp_gemm_workspace_bytes_mnk(M, N, K);
+    if (ws && ws_aligned && need_p > 0 && workspace_bytes >= need_p) {
+        const int64_t Kp = (K + 7) / 8 * 8;
+        uint16_t* hi = ws;
+        uint16_t* lo = ws + M * Kp;
+        uint16_t* wp = ws + 2 * M * Kp;
+        comp_status_t r = launch_split_padded(x, hi, lo, M, K, Kp, dev, s);
+        if (r == COMP_OK)
+            r = launch_pad_rows(W, wp, N, K, Kp, dev, s);
+        if (r != COMP_OK)
+            return r;
+        return launch_gemm_f16x2(hi, lo, wp, y, M, N, Kp, 0, dev, s, epi);
+    }
+    return launch_gemm_tc(x, W, y, M, N, K, 0, dev, s, epi);
+}
+
+comp_status_t gemm_f16x2_impl(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
+                              int64_t N, int64_t K, int variant, comp_stream_t stream, const Epilogue& epi)
+{
+    DeviceInfo dev;
+    bool empty;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (variant < 0 || variant > 3 || (variant == 3 && M > 32))
+        return COMP_ERR_INVALID_VALUE;
+    const comp_status_t st = check_gemm(hi, 2, W, y, M, N, K, s, &dev, &empty);
+    if (st != COMP_OK || empty)
+        return st;
+    // check_gemm has bounded M*N and M*K
+    if (!lo || overlap(y, 4 * M * N, lo, 2 * M * K))
+        return COMP_ERR_INVALID_VALUE;
+    if (!gemm_f16x2_supported(hi, lo, W, K))
+        return COMP_ERR_INVALID_VALUE;
+    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, variant, dev, s, epi);
+}
+
 }  // namespace
 }  // namespace compfp32
 
@@ -175,20 +255,7 @@ comp_status_t comp_gemm_f32_simt(const float* x, const uint16_t* W, float* y, in
 comp_status_t comp_gemm_f16x2_variant(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
                                       int64_t N, int64_t K, int variant, comp_stream_t stream)
 {
-    DeviceInfo dev;
-    bool empty;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (variant < 0 || variant > 3 || (variant == 3 && M > 32))
-        return COMP_ERR_INVALID_VALUE;
-    const comp_status_t st = check_gemm(hi, 2, W, y, M, N, K, s, &dev, &empty);
-    if (st != COMP_OK || empty)
-        return st;
-    // check_gemm has bounded M*N and M*K
-    if (!lo || overlap(y, 4 * M * N, lo, 2 * M * K))
-        return COMP_ERR_INVALID_VALUE;
-    if (!gemm_f16x2_supported(hi, lo, W, K))
-        return COMP_ERR_INVALID_VALUE;
-    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, variant, dev, s);
+    return gemm_f16x2_impl(hi, lo, W, y, M, N, K, variant, stream, Epilogue{});
 }
 
 comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
@@ -220,49 +287,28 @@ int64_t comp_gemm_workspace_bytes_mnk(int64_t M, int64_t N, int64_t K)
 comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                   void* workspace, int64_t workspace_bytes, comp_stream_t stream)
 {
-    DeviceInfo dev;
-    bool empty;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const comp_status_t st = check_gemm(x, 4, W, y, M, N, K, s, &dev, &empty);
-    if (st != COMP_OK || empty)
-        return st;
-    if (workspace_bytes < 0 || (workspace_bytes > 0 && !workspace))
-        return COMP_ERR_INVALID_VALUE;
-    if (workspace && workspace_bytes > 0 &&
-        (overlap(workspace, workspace_bytes, x, 4 * M * K) || overlap(workspace, workspace_bytes, W, 2 * N * K) ||
-         overlap(workspace, workspace_bytes, y, 4 * M * N)))
-        return COMP_ERR_INVALID_VALUE;
-    // at most 32 rows against a wide W: one kernel with the split fused needs
-    // no workspace and is faster than the two-pass form
-    if (swap_fused_preferred(x, W, M, N, K))
-        return launch_swap_fused(x, W, y, M, N, K, dev, s);
-    uint16_t* const ws = static_cast<uint16_t*>(workspace);
-    const bool ws_aligned = (reinterpret_cast<uintptr_t>(workspace) & 15u) == 0;
-    // two-pass form on the caller's W: planes [M, K] in the workspace
-    const int64_t need = comp_gemm_workspace_bytes(M, K);
-    if (ws && ws_aligned && need > 0 && workspace_bytes >= need && gemm_f16x2_supported(ws, ws + M * K, W, K)) {
-        const comp_status_t sp = launch_split(x, ws, ws + M * K, M * K, dev, s);
-        if (sp != COMP_OK)
-            return sp;
-        return launch_gemm_f16x2(ws, ws + M * K, W, y, M, N, K, 0, dev, s);
-    }
-    // two-pass form with K padded to a multiple of 8 (any K, any alignment):
-    // planes [M, Kp] and a zero-padded copy of W [N, Kp] in the workspace
-    const int64_t need_p = comp_gemm_workspace_bytes_mnk(M, N, K);
-    if (ws && ws_aligned && need_p > 0 && workspace_bytes >= need_p) {
-        const int64_t Kp = (K + 7) / 8 * 8;
-        uint16_t* hi = ws;
-        uint16_t* lo = ws + M * Kp;
-        uint16_t* wp = ws + 2 * M * Kp;
-        comp_status_t r = launch_split_padded(x, hi, lo, M, K, Kp, dev, s);
-        if (r == COMP_OK)
-            r = launch_pad_rows(W, wp, N, K, Kp, dev, s);
-        if (r != COMP_OK)
-            return r;
-        return launch_gemm_f16x2(hi, lo, wp, y, M, N, Kp, 0, dev, s);
-    }
-    return launch_gemm_tc(x, W, y, M, N, K, 0, dev, s);
+    return gemm_ws_impl(x, W, y, M, N, K, workspace, workspace_bytes, stream, Epilogue{});
 }
+
+comp_status_t comp_gemm_f32x16_epilogue(const float* x, const uint16_t* W, const float* bias, const float* gate,
+                                        float* y, int64_t M, int64_t N, int64_t K, void* workspace,
+                                        int64_t workspace_bytes, comp_stream_t stream)
+{
+    if (!epilogue_args_ok(bias, gate, y, M, N))
+        return COMP_ERR_INVALID_VALUE;
+    return gemm_ws_impl(x, W, y, M, N, K, workspace, workspace_bytes, stream, Epilogue{bias, gate});
+}
+
+comp_status_t comp_gemm_f16x2_epilogue(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, const float* bias,
+                                       const float* gate, float* y, int64_t M, int64_t N, int64_t K, int variant,
+                                       comp_stream_t stream)
+{
+    if (!epilogue_args_ok(bias, gate, y, M, N))
+        return COMP_ERR_INVALID_VALUE;
+    return gemm_f16x2_impl(hi, lo, W, y, M, N, K, variant, stream, Epilogue{bias, gate});
+}
+
+
 
 comp_status_t comp_check_wait_timeout(comp_stream_t stream)
 {

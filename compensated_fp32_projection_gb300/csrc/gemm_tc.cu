@@ -288,8 +288,27 @@ struct Problem {
     int M, N, K;
     int tiles_m, tiles_n, nk;
     int vec_y;
-    int tma_y;  // y is written with tensor-map stores (kernels that support it)
+    int tma_y;                     // y is written with tensor-map stores (kernels that support it)
+    const float* bias = nullptr;   // epilogue: [N], added to y (nullptr: none)
+    const float* gate = nullptr;   // epilogue: [M, N], y times gelu(gate) (nullptr: factor 1)
 };
+
+// Epilogue of a GEGLU feed-forward step (laya.cpp docs/vulkan.md, feed-forward
+// paragraph: gate activation and multiplication fused into one dispatch), on
+// element (m, n) of the merged projection: gelu(gate) * (y + bias), with the
+// exact GELU g * Phi(g), Phi(g) = erfc(-g / sqrt 2) / 2 (no cancellation for
+// negative g).  Each operation rounds to nearest even; never contracted.
+__device__ __forceinline__ float epilogue_at(float v, int64_t m, int64_t n, const Problem& P)
+{
+    if (P.bias)
+        v = __fadd_rn(v, __ldg(P.bias + n));
+    if (P.gate) {
+        const float g = __ldg(P.gate + m * static_cast<int64_t>(P.N) + n);
+        const float phi = __fmul_rn(0.5f, erfcf(__fmul_rn(-g, 0.70710678118654752f)));  // 1 / sqrt 2
+        v = __fmul_rn(v, __fmul_rn(g, phi));
+    }
+    return v;
+}
 
 // Tile t covers rows (t / tiles_n) * 128 .. and columns (t % tiles_n) * BN ..;
 // N runs fastest so that CTAs working at the same time share rows of x.
@@ -482,6 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t m = static_cast<int64_t>(cur.m0) + wq * 32 + lane;
                 const int64_t nb = static_cast<int64_t>(cur.n0) + wh * C::kHalf;
                 if (m < P.M) {
+                    if (P.bias || P.gate) {
+#pragma unroll
+                        for (int i = 0; i < C::kHalf; ++i)
+                            if (nb + i < P.N)
+                                R[i] = epilogue_at(R[i], m, nb + i, P);
+                    }
                     float* yrow = P.y + m * P.N;
                     if (P.vec_y && nb + C::kHalf <= P.N) {
 #pragma unroll
@@ -962,6 +987,12 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
                     const int64_t m = static_cast<int64_t>(tile_m(t, P)) * BM + wq * 32 + lane;
                     const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
                     if (m < P.M && *reinterpret_cast<volatile int*>(&bars->abort) == 0) {
+                        if (P.bias || P.gate) {
+#pragma unroll
+                            for (int i = 0; i < C::kHalf; ++i)
+                                if (nb + i < P.N)
+                                    R[i] = epilogue_at(R[i], m, nb + i, P);
+                        }
                         float* yrow = P.y + m * P.N;
                         if (P.vec_y && nb + C::kHalf <= P.N) {
 #pragma unroll
@@ -1296,6 +1327,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                 const int64_t row0 = static_cast<int64_t>(tile_m(t, P)) * pair::kRows + rank * BM + wq * 32;
                 const int64_t m = row0 + lane;
                 const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
+                if ((P.bias || P.gate) && m < P.M) {
+#pragma unroll
+                    for (int i = 0; i < C::kHalf; ++i)
+                        if (nb + i < P.N)
+                            R[i] = epilogue_at(R[i], m, nb + i, P);
+                }
                 if (P.tma_y) {
                     // 16-column pieces through shared memory; the tensor-map store
                     // clips rows >= M and columns >= N
@@ -1631,7 +1668,8 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
 #pragma unroll
                     for (int m = 0; m < MP; ++m)
                         if (m < P.M)
-                            P.y[m * static_cast<int64_t>(P.N) + col] = __fadd_rn(Rh[m], __fmul_rn(Rl[m], 0x1p-10f));
+                            P.y[m * static_cast<int64_t>(P.N) + col] =
+                                epilogue_at(__fadd_rn(Rh[m], __fmul_rn(Rl[m], 0x1p-10f)), m, col, P);
                 }
 #pragma unroll
                 for (int i = 0; i < MP; ++i) {
@@ -1759,7 +1797,7 @@ comp_status_t dispatch(int bn, const CUtensorMap& tw, const CUtensorMap& tx, con
 }  // namespace
 
 comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
-                             int variant, const DeviceInfo& dev, cudaStream_t stream)
+                             int variant, const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi)
 {
     const bool vec_ok = aligned16(x) && aligned16(W) && (K % 8 == 0);
     // at most 32 rows: the swapped-operand kernel with the split fused (variant
@@ -1767,7 +1805,7 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
     if (variant == 3 || (variant == 0 && swap_fused_preferred(x, W, M, N, K))) {
         if (!vec_ok || M > 32)
             return COMP_ERR_INVALID_VALUE;
-        return launch_swap_fused(x, W, y, M, N, K, dev, stream);
+        return launch_swap_fused(x, W, y, M, N, K, dev, stream, epi);
     }
     if (variant == 1 && !vec_ok)
         return COMP_ERR_INVALID_VALUE;
@@ -1783,6 +1821,8 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
     P.nk = static_cast<int>((K + BK - 1) / BK);
     P.vec_y = (N % 4 == 0) && aligned16(y);
     P.tma_y = 0;
+    P.bias = epi.bias;
+    P.gate = epi.gate;
     const int bn = pick_bn(M, N, dev.sm_count);
     P.tiles_m = static_cast<int>((M + BM - 1) / BM);
     P.tiles_n = static_cast<int>((N + bn - 1) / bn);
@@ -2011,7 +2051,8 @@ bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t
 }
 
 comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
-                                int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream)
+                                int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream,
+                                const Epilogue& epi)
 {
     if (!gemm_f16x2_supported(hi, lo, W, K) || variant < 0 || variant > 3 || (variant == 3 && M > 32))
         return COMP_ERR_INVALID_VALUE;
@@ -2028,6 +2069,8 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     P.nk = static_cast<int>((K + BK - 1) / BK);
     P.vec_y = (N % 4 == 0) && aligned16(y);
     P.tma_y = 0;
+    P.bias = epi.bias;
+    P.gate = epi.gate;
     CUtensorMap th{}, tl{}, tw{};
     // at most 32 rows and at least 32 tiles of 128 columns: operands swapped,
     // W streams through full 128-row MMAs
@@ -2112,7 +2155,7 @@ bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t 
 }
 
 comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
-                                const DeviceInfo& dev, cudaStream_t stream)
+                                const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi)
 {
     if (M > 32 || K % 8 != 0 || !aligned16(x) || !aligned16(W))
         return COMP_ERR_INVALID_VALUE;
@@ -2126,6 +2169,8 @@ comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int
     P.nk = static_cast<int>((K + BK - 1) / BK);
     P.vec_y = (N % 4 == 0) && aligned16(y);
     P.tma_y = 0;
+    P.bias = epi.bias;
+    P.gate = epi.gate;
     P.tiles_m = 1;
     P.tiles_n = static_cast<int>((N + swp::kTileN - 1) / swp::kTileN);
     if (static_cast<int64_t>(P.tiles_n) * P.nk > INT32_MAX / 2)

@@ -31,13 +31,20 @@ comp_status_t launch_merge(const float* acc_hi, const float* acc_lo, float* y, i
 comp_status_t launch_gemm_simt(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                const DeviceInfo& dev, cudaStream_t stream);
 // variant: 0 automatic, 1 TMA loads, 2 plain loads.
+// Optional FP32 operations on the merged projection in the product kernels'
+// epilogue (GEGLU feed-forward step): y = gelu(gate) * (y + bias).
+struct Epilogue {
+    const float* bias = nullptr;  // [N] (nullptr: none)
+    const float* gate = nullptr;  // [M, N] row-major (nullptr: factor 1)
+};
+
 // Fused split and swapped-operand product for at most 32 rows of x (K a
 // multiple of 8, x and W 16-byte aligned); preferred once N spans 32 tiles of 128.
 bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K);
 comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
-                                const DeviceInfo& dev, cudaStream_t stream);
+                                const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi = Epilogue{});
 comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
-                             int variant, const DeviceInfo& dev, cudaStream_t stream);
+                             int variant, const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi = Epilogue{});
 
 // The two products and the merge from split planes (hi, lo: [M, K] FP16).
 // Needs 16-byte aligned hi, lo, W and K % 8 == 0 (else COMP_ERR_INVALID_VALUE).
@@ -45,7 +52,8 @@ bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t
 // variant: 0 automatic, 1 one CTA per 128-row tile, 2 CTA pairs on 256-row
 // tiles, 3 operands swapped (M <= 32).
 comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
-                                int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream);
+                                int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream,
+                                const Epilogue& epi = Epilogue{});
 
 // One thread runs a bounded wait that cannot succeed (comp_check_wait_timeout).
 comp_status_t launch_check_wait_timeout(cudaStream_t stream);

@@ -200,6 +200,39 @@ comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, i
                                   void* workspace, int64_t workspace_bytes, comp_stream_t stream);
 
 /*
+ * comp_gemm_f32x16_epilogue — the projection of comp_gemm_f32x16_ws followed,
+ * inside the product kernel's epilogue, by the FP32 operations of a GEGLU
+ * feed-forward step (laya.cpp docs/vulkan.md, feed-forward paragraph: the gate
+ * activation and multiplication are fused into one dispatch, with no separate
+ * copies or passes):
+ *   out[m,n] = gelu(gate[m,n]) * (y[m,n] + bias[n]),
+ *   gelu(g) = g * Phi(g), Phi(g) = erfc(-g / sqrt 2) / 2 (the exact GELU),
+ * with y the compensated projection.  Each operation is an FP32 operation
+ * rounded to nearest even; erfc is CUDA's erfcf.
+ *   bias : [N] binary32, or NULL for none (input).
+ *   gate : [M, N] binary32 row-major, or NULL for a factor of 1 (input), e.g.
+ *          the gate projection of the same x computed by an earlier call.
+ *   out is written to y.  A GEGLU layer is then two calls: gate = x W_g^T + b_g
+ *   (this call with gate NULL), then y = gelu(gate) * (x W_u^T + b_u).
+ * Workspace, alignment and path rules are those of comp_gemm_f32x16_ws.
+ * Errors: those of comp_gemm_f32x16_ws; COMP_ERR_INVALID_VALUE also if bias or
+ * gate overlaps y.
+ */
+comp_status_t comp_gemm_f32x16_epilogue(const float* x, const uint16_t* W, const float* bias, const float* gate,
+                                        float* y, int64_t M, int64_t N, int64_t K, void* workspace,
+                                        int64_t workspace_bytes, comp_stream_t stream);
+
+/*
+ * comp_gemm_f16x2_epilogue — comp_gemm_f16x2_variant (from the split planes,
+ * kernel chosen by `variant` as there) with the epilogue of
+ * comp_gemm_f32x16_epilogue.  Same errors as comp_gemm_f16x2_variant, plus
+ * COMP_ERR_INVALID_VALUE if bias or gate overlaps y.
+ */
+comp_status_t comp_gemm_f16x2_epilogue(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, const float* bias,
+                                       const float* gate, float* y, int64_t M, int64_t N, int64_t K, int variant,
+                                       comp_stream_t stream);
+
+/*
  * COMP_NOALLOC_MAX_WORKSPACE_BYTES — size of the static device workspace of
  * comp_gemm_f32x16_noalloc: 64 MiB, i.e. 4 * M * K <= 67108864
  * (M * K <= 16777216, e.g. a 4096 x 4096 activation).

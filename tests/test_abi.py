@@ -105,6 +105,19 @@ def test_two_pass_argument_errors(lib):
     assert ws(None, None, None, 0, 4, 4, None, 0, None) == 0
 
 
+def test_epilogue_argument_errors(lib):
+    ep, e2 = lib.comp_gemm_f32x16_epilogue, lib.comp_gemm_f16x2_epilogue
+    # comp_gemm_f32x16_epilogue(x, W, bias, gate, y, M, N, K, workspace, bytes, stream): 4 x 8 output at 1 << 24
+    y = 1 << 24
+    assert ep(P(4096), P(1 << 20), P(y + 4), None, P(y), 4, 8, 8, None, 0, None) == 1  # bias overlaps y
+    assert ep(P(4096), P(1 << 20), None, P(y + 64), P(y), 4, 8, 8, None, 0, None) == 1  # gate overlaps y
+    assert ep(P(4096), P(1 << 20), None, None, P(y), -1, 8, 8, None, 0, None) == 1
+    assert ep(None, None, None, None, None, 0, 8, 8, None, 0, None) == 0  # empty output: no-op
+    # comp_gemm_f16x2_epilogue(hi, lo, W, bias, gate, y, M, N, K, variant, stream)
+    assert e2(P(4096), P(1 << 16), P(1 << 20), P(y + 28), None, P(y), 4, 8, 8, 0, None) == 1
+    assert e2(P(4096), P(1 << 16), P(1 << 20), None, None, P(y), 4, 8, 8, 4, None) == 1  # variant out of range
+
+
 def test_workspace_bytes_mnk(lib):
     assert lib.comp_gemm_workspace_bytes_mnk(1000, 771, 1027) == 4 * 1000 * 1032 + 2 * 771 * 1032
     assert lib.comp_gemm_workspace_bytes_mnk(4096, 4096, 4096) == 4 * 4096 * 4096 + 2 * 4096 * 4096
