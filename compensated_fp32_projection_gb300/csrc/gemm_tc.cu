@@ -310,6 +310,57 @@ __device__ __forceinline__ float epilogue_at(float v, int64_t m, int64_t n, cons
     return v;
 }
 
+// The epilogue on 16 consecutive columns n0.. of row m, held in v[0..15];
+// columns >= N are left as they are.  The bias and gate values are all loaded
+// first (16-byte loads where the row segment allows), then combined, so that
+// a thread waits for one round of loads per 16 columns.  Same operations as
+// epilogue_at.
+__device__ __forceinline__ void epilogue16(float* v, int64_t m, int64_t n0, const Problem& P)
+{
+    float b[16], f[16];  // bias, then the gate's gelu factors
+    const bool full = n0 + 16 <= P.N;
+    const float* grow = P.gate ? P.gate + m * static_cast<int64_t>(P.N) + n0 : nullptr;
+    if (P.bias) {
+        if (full && (reinterpret_cast<uintptr_t>(P.bias + n0) & 15u) == 0) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(b + i) = __ldg(reinterpret_cast<const float4*>(P.bias + n0 + i));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                b[i] = n0 + i < P.N ? __ldg(P.bias + n0 + i) : 0.0f;
+        }
+    }
+    if (grow) {
+        if (full && (reinterpret_cast<uintptr_t>(grow) & 15u) == 0) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+                *reinterpret_cast<float4*>(f + i) = __ldg(reinterpret_cast<const float4*>(grow + i));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                f[i] = n0 + i < P.N ? __ldg(grow + i) : 0.0f;
+        }
+        // one copy of the GELU arithmetic: a loop kept rolled over the 16 factors
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            const float g = f[i];
+            f[i] = __fmul_rn(g, __fmul_rn(0.5f, erfcf(__fmul_rn(-g, 0.70710678118654752f))));  // 1 / sqrt 2
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        if (n0 + i < P.N) {
+            float x = v[i];
+            if (P.bias)
+                x = __fadd_rn(x, b[i]);
+            if (grow)
+                x = __fmul_rn(x, f[i]);
+            v[i] = x;
+        }
+    }
+}
+
 // Tile t covers rows (t / tiles_n) * 128 .. and columns (t % tiles_n) * BN ..;
 // N runs fastest so that CTAs working at the same time share rows of x.
 __device__ __forceinline__ int tile_m(int t, const Problem& P)
@@ -344,7 +395,7 @@ struct Cursor {
     }
 };
 
-template <int BN, bool kVec>
+template <int BN, bool kVec, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     comp_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                      const Problem P)
@@ -501,11 +552,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t m = static_cast<int64_t>(cur.m0) + wq * 32 + lane;
                 const int64_t nb = static_cast<int64_t>(cur.n0) + wh * C::kHalf;
                 if (m < P.M) {
-                    if (P.bias || P.gate) {
+                    if constexpr (EPI) {
+                        static_assert(C::kHalf % 16 == 0, "epilogue in pieces of 16 columns");
 #pragma unroll
-                        for (int i = 0; i < C::kHalf; ++i)
-                            if (nb + i < P.N)
-                                R[i] = epilogue_at(R[i], m, nb + i, P);
+                        for (int p = 0; p < C::kHalf; p += 16)
+                            epilogue16(R + p, m, nb + p, P);
                     }
                     float* yrow = P.y + m * P.N;
                     if (P.vec_y && nb + C::kHalf <= P.N) {
@@ -705,7 +756,7 @@ constexpr uint32_t kFaultX2Reduce = 0x505;
 // sums are added in rank order in the leader (deterministic, no atomics, no
 // global scratch).  Split K is used for problems of at most 32 rows, whose
 // valid rows all sit in TMEM lanes 0..31 (promotion warps 4 and 8).
-template <int BN, int NS, int CH, int AR, int KS>
+template <int BN, int NS, int CH, int AR, int KS, bool EPI>
 __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, const CUtensorMap& tmap_lo,
                                                 const CUtensorMap& tmap_w, const Problem& P)
 {
@@ -987,11 +1038,11 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
                     const int64_t m = static_cast<int64_t>(tile_m(t, P)) * BM + wq * 32 + lane;
                     const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
                     if (m < P.M && *reinterpret_cast<volatile int*>(&bars->abort) == 0) {
-                        if (P.bias || P.gate) {
+                        if constexpr (EPI) {
+                            static_assert(C::kHalf % 16 == 0, "epilogue in pieces of 16 columns");
 #pragma unroll
-                            for (int i = 0; i < C::kHalf; ++i)
-                                if (nb + i < P.N)
-                                    R[i] = epilogue_at(R[i], m, nb + i, P);
+                            for (int p = 0; p < C::kHalf; p += 16)
+                                epilogue16(R + p, m, nb + p, P);
                         }
                         float* yrow = P.y + m * P.N;
                         if (P.vec_y && nb + C::kHalf <= P.N) {
@@ -1027,20 +1078,20 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
     }
 }
 
-template <int BN, int NS, int CH, int AR>
+template <int BN, int NS, int CH, int AR, bool EPI>
 __global__ void __launch_bounds__(x2::kThreads, 1)
     comp_f16x2_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
                       const __grid_constant__ CUtensorMap tmap_w, const Problem P)
 {
-    f16x2_tile_body<BN, NS, CH, AR, 1>(tmap_hi, tmap_lo, tmap_w, P);
+    f16x2_tile_body<BN, NS, CH, AR, 1, EPI>(tmap_hi, tmap_lo, tmap_w, P);
 }
 
-template <int BN, int NS, int CH, int AR, int KS>
+template <int BN, int NS, int CH, int AR, int KS, bool EPI>
 __global__ void __cluster_dims__(KS, 1, 1) __launch_bounds__(x2::kThreads, 1)
     comp_f16x2_splitk_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
                              const __grid_constant__ CUtensorMap tmap_w, const Problem P)
 {
-    f16x2_tile_body<BN, NS, CH, AR, KS>(tmap_hi, tmap_lo, tmap_w, P);
+    f16x2_tile_body<BN, NS, CH, AR, KS, EPI>(tmap_hi, tmap_lo, tmap_w, P);
 }
 
 // ---------------------------------------------------------------------------
@@ -1111,7 +1162,8 @@ constexpr uint32_t kFaultPairProducer = 0x701;
 constexpr uint32_t kFaultPairMma = 0x702;
 constexpr uint32_t kFaultPairPromote = 0x703;
 
-template <int BN, int NS, int CH>
+
+template <int BN, int NS, int CH, bool EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     comp_f16x2_pair_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
                            const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_y,
@@ -1327,11 +1379,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                 const int64_t row0 = static_cast<int64_t>(tile_m(t, P)) * pair::kRows + rank * BM + wq * 32;
                 const int64_t m = row0 + lane;
                 const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
-                if ((P.bias || P.gate) && m < P.M) {
+                if constexpr (EPI) {
+                    static_assert(C::kHalf % 16 == 0, "epilogue in pieces of 16 columns");
+                    if (m < P.M) {
 #pragma unroll
-                    for (int i = 0; i < C::kHalf; ++i)
-                        if (nb + i < P.N)
-                            R[i] = epilogue_at(R[i], m, nb + i, P);
+                        for (int p = 0; p < C::kHalf; p += 16)
+                            epilogue16(R + p, m, nb + p, P);
+                    }
                 }
                 if (P.tma_y) {
                     // 16-column pieces through shared memory; the tensor-map store
@@ -1462,7 +1516,7 @@ constexpr uint32_t kFaultSwpPromote = 0x803;
 constexpr uint32_t kFaultSwpSplit = 0x804;
 
 // FX: tmap_hi is the map of FP32 x (boxes of 64 x Mp, no swizzle); tmap_lo is unused.
-template <int MP, int BPS, int NS, bool FX>
+template <int MP, int BPS, int NS, bool FX, bool EPI>
 __global__ void __launch_bounds__(swp::kThreads, 1)
     comp_f16x2_swap_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
                            const __grid_constant__ CUtensorMap tmap_w, const Problem P)
@@ -1668,8 +1722,10 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
 #pragma unroll
                     for (int m = 0; m < MP; ++m)
                         if (m < P.M)
-                            P.y[m * static_cast<int64_t>(P.N) + col] =
-                                epilogue_at(__fadd_rn(Rh[m], __fmul_rn(Rl[m], 0x1p-10f)), m, col, P);
+                        {
+                            const float v = __fadd_rn(Rh[m], __fmul_rn(Rl[m], 0x1p-10f));
+                            P.y[m * static_cast<int64_t>(P.N) + col] = EPI ? epilogue_at(v, m, col, P) : v;
+                        }
                 }
 #pragma unroll
                 for (int i = 0; i < MP; ++i) {
@@ -1732,9 +1788,9 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, size_t elem, const v
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool kVec>
-comp_status_t launch_bn(const CUtensorMap& tw, const CUtensorMap& tx, const Problem& P, const DeviceInfo& dev,
-                        cudaStream_t stream)
+template <int BN, bool kVec, bool EPI>
+comp_status_t launch_bn_t(const CUtensorMap& tw, const CUtensorMap& tx, const Problem& P, const DeviceInfo& dev,
+                          cudaStream_t stream)
 {
     static std::mutex mu;
     static bool done[64] = {};
@@ -1743,7 +1799,7 @@ comp_status_t launch_bn(const CUtensorMap& tw, const CUtensorMap& tx, const Prob
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (!done[dev.device]) {
-            if (cudaFuncSetAttribute(comp_gemm_kernel<BN, kVec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(comp_gemm_kernel<BN, kVec, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(Cfg<BN>::kSmem)) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return COMP_ERR_CUDA;
@@ -1753,8 +1809,17 @@ comp_status_t launch_bn(const CUtensorMap& tw, const CUtensorMap& tx, const Prob
     }
     const int tiles = P.tiles_m * P.tiles_n;
     const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-    comp_gemm_kernel<BN, kVec><<<grid, kThreads, Cfg<BN>::kSmem, stream>>>(tw, tx, P);
+    comp_gemm_kernel<BN, kVec, EPI><<<grid, kThreads, Cfg<BN>::kSmem, stream>>>(tw, tx, P);
     return launch_status();
+}
+
+// The instance with the epilogue compiled in only when the call has one.
+template <int BN, bool kVec>
+comp_status_t launch_bn(const CUtensorMap& tw, const CUtensorMap& tx, const Problem& P, const DeviceInfo& dev,
+                        cudaStream_t stream)
+{
+    return (P.bias || P.gate) ? launch_bn_t<BN, kVec, true>(tw, tx, P, dev, stream)
+                              : launch_bn_t<BN, kVec, false>(tw, tx, P, dev, stream);
 }
 
 // The N tile width expected to finish first: rounds of tiles over the SMs
@@ -1866,9 +1931,9 @@ comp_status_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t
     return COMP_OK;
 }
 
-template <int BN, int NS, int CH, int AR, int KS>
-comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
-                               const DeviceInfo& dev, cudaStream_t stream)
+template <int BN, int NS, int CH, int AR, int KS, bool EPI>
+comp_status_t launch_x2_splitk_t(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+                                 const DeviceInfo& dev, cudaStream_t stream)
 {
     using C = x2::Cfg<BN, NS, CH, AR, KS>;
     static std::mutex mu;
@@ -1879,7 +1944,7 @@ comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, con
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (clusters[dev.device] == 0) {
-            if (cudaFuncSetAttribute(comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS>,
+            if (cudaFuncSetAttribute(comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS, EPI>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(C::kSmem)) != cudaSuccess) {
                 (void)cudaGetLastError();
@@ -1890,7 +1955,7 @@ comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, con
             cfg.blockDim = dim3(x2::kThreads, 1, 1);
             cfg.dynamicSmemBytes = C::kSmem;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS>, &cfg) !=
+            if (cudaOccupancyMaxActiveClusters(&n, comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS, EPI>, &cfg) !=
                     cudaSuccess ||
                 n <= 0) {
                 (void)cudaGetLastError();
@@ -1902,12 +1967,20 @@ comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, con
     }
     const int tiles = P.tiles_m * P.tiles_n;
     const int grid = KS * (tiles < nc ? tiles : nc);
-    return launch_pdl(comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS>, grid, x2::kThreads, C::kSmem, stream, th, tl, tw,
+    return launch_pdl(comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS, EPI>, grid, x2::kThreads, C::kSmem, stream, th, tl, tw,
                       P);
 }
 
-template <int MP, int BPS, int NS, bool FX = false>
-comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+template <int BN, int NS, int CH, int AR, int KS>
+comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+                               const DeviceInfo& dev, cudaStream_t stream)
+{
+    return (P.bias || P.gate) ? launch_x2_splitk_t<BN, NS, CH, AR, KS, true>(th, tl, tw, P, dev, stream)
+                              : launch_x2_splitk_t<BN, NS, CH, AR, KS, false>(th, tl, tw, P, dev, stream);
+}
+
+template <int MP, int BPS, int NS, bool FX, bool EPI>
+comp_status_t launch_swap_t(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                           const DeviceInfo& dev, cudaStream_t stream)
 {
     using C = swp::Cfg<MP, BPS, NS, FX>;
@@ -1918,7 +1991,7 @@ comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CU
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (!done[dev.device]) {
-            if (cudaFuncSetAttribute(comp_f16x2_swap_kernel<MP, BPS, NS, FX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(comp_f16x2_swap_kernel<MP, BPS, NS, FX, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(C::kSmem)) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return COMP_ERR_CUDA;
@@ -1927,12 +2000,20 @@ comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CU
         }
     }
     const int grid = P.tiles_n < dev.sm_count ? P.tiles_n : dev.sm_count;
-    return launch_pdl(comp_f16x2_swap_kernel<MP, BPS, NS, FX>, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
+    return launch_pdl(comp_f16x2_swap_kernel<MP, BPS, NS, FX, EPI>, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
 }
 
-template <int BN, int NS, int CH, int AR = BM>
-comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
-                           const DeviceInfo& dev, cudaStream_t stream)
+template <int MP, int BPS, int NS, bool FX = false>
+comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+                          const DeviceInfo& dev, cudaStream_t stream)
+{
+    return (P.bias || P.gate) ? launch_swap_t<MP, BPS, NS, FX, true>(th, tl, tw, P, dev, stream)
+                              : launch_swap_t<MP, BPS, NS, FX, false>(th, tl, tw, P, dev, stream);
+}
+
+template <int BN, int NS, int CH, int AR, bool EPI>
+comp_status_t launch_x2_bn_t(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+                             const DeviceInfo& dev, cudaStream_t stream)
 {
     using C = x2::Cfg<BN, NS, CH, AR>;
     static std::mutex mu;
@@ -1942,7 +2023,7 @@ comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const C
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (!done[dev.device]) {
-            if (cudaFuncSetAttribute(comp_f16x2_kernel<BN, NS, CH, AR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(comp_f16x2_kernel<BN, NS, CH, AR, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(C::kSmem)) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return COMP_ERR_CUDA;
@@ -1952,11 +2033,19 @@ comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const C
     }
     const int tiles = P.tiles_m * P.tiles_n;
     const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-    return launch_pdl(comp_f16x2_kernel<BN, NS, CH, AR>, grid, x2::kThreads, C::kSmem, stream, th, tl, tw, P);
+    return launch_pdl(comp_f16x2_kernel<BN, NS, CH, AR, EPI>, grid, x2::kThreads, C::kSmem, stream, th, tl, tw, P);
 }
 
-template <int BN, int NS, int CH>
-comp_status_t launch_pair_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const CUtensorMap& ty,
+template <int BN, int NS, int CH, int AR = BM>
+comp_status_t launch_x2_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+                           const DeviceInfo& dev, cudaStream_t stream)
+{
+    return (P.bias || P.gate) ? launch_x2_bn_t<BN, NS, CH, AR, true>(th, tl, tw, P, dev, stream)
+                              : launch_x2_bn_t<BN, NS, CH, AR, false>(th, tl, tw, P, dev, stream);
+}
+
+template <int BN, int NS, int CH, bool EPI>
+comp_status_t launch_pair_bn_t(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const CUtensorMap& ty,
                              const Problem& P, const DeviceInfo& dev, cudaStream_t stream)
 {
     using C = pair::Cfg<BN, NS, CH>;
@@ -1968,7 +2057,7 @@ comp_status_t launch_pair_bn(const CUtensorMap& th, const CUtensorMap& tl, const
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (pairs[dev.device] == 0) {
-            if (cudaFuncSetAttribute(comp_f16x2_pair_kernel<BN, NS, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(comp_f16x2_pair_kernel<BN, NS, CH, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(C::kSmem)) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return COMP_ERR_CUDA;
@@ -1978,7 +2067,7 @@ comp_status_t launch_pair_bn(const CUtensorMap& th, const CUtensorMap& tl, const
             cfg.blockDim = dim3(pair::kThreads, 1, 1);
             cfg.dynamicSmemBytes = C::kSmem;
             int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, comp_f16x2_pair_kernel<BN, NS, CH>, &cfg) != cudaSuccess ||
+            if (cudaOccupancyMaxActiveClusters(&clusters, comp_f16x2_pair_kernel<BN, NS, CH, EPI>, &cfg) != cudaSuccess ||
                 clusters <= 0) {
                 (void)cudaGetLastError();
                 clusters = dev.sm_count / 2;
@@ -1989,7 +2078,15 @@ comp_status_t launch_pair_bn(const CUtensorMap& th, const CUtensorMap& tl, const
     }
     const int tiles = P.tiles_m * P.tiles_n;
     const int grid = 2 * (tiles < np ? tiles : np);
-    return launch_pdl(comp_f16x2_pair_kernel<BN, NS, CH>, grid, pair::kThreads, C::kSmem, stream, th, tl, tw, ty, P);
+    return launch_pdl(comp_f16x2_pair_kernel<BN, NS, CH, EPI>, grid, pair::kThreads, C::kSmem, stream, th, tl, tw, ty, P);
+}
+
+template <int BN, int NS, int CH>
+comp_status_t launch_pair_bn(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const CUtensorMap& ty,
+                             const Problem& P, const DeviceInfo& dev, cudaStream_t stream)
+{
+    return (P.bias || P.gate) ? launch_pair_bn_t<BN, NS, CH, true>(th, tl, tw, ty, P, dev, stream)
+                              : launch_pair_bn_t<BN, NS, CH, false>(th, tl, tw, ty, P, dev, stream);
 }
 
 // N tile width for the two-pass product (tiles are all tensor work there).
