@@ -25,6 +25,7 @@ __all__ = [
     "comp_gemm_f16x2",
     "comp_gemm_f16x2_variant",
     "comp_gemm_f32x16_ws",
+    "comp_geglu_f32",
     "comp_gemm_f32x16_epilogue",
     "comp_gemm_f16x2_epilogue",
     "comp_gemm_workspace_bytes",
@@ -181,6 +182,22 @@ def comp_gemm_f32x16_ws(x, W, y=None, workspace=None, stream=None):
     _native.call("comp_gemm_f32x16_ws", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K, workspace.data_ptr(),
                  nbytes, _stream(x, stream))
     return y
+
+
+def comp_geglu_f32(gate, up, out=None, stream=None):
+    """out = gelu(gate) * up elementwise (exact GELU), one dispatch; out may be gate or up."""
+    torch = _torch()
+    _check(gate, torch.float32, "gate")
+    _check(up, torch.float32, "up")
+    if gate.shape != up.shape or gate.device != up.device:
+        raise ValueError("gate and up must have the same shape and device")
+    if out is None:
+        out = torch.empty_like(up)
+    _check(out, torch.float32, "out")
+    if out.shape != up.shape:
+        raise ValueError("out must have the shape of up")
+    _native.call("comp_geglu_f32", gate.data_ptr(), up.data_ptr(), out.data_ptr(), up.numel(), _stream(up, stream))
+    return out
 
 
 def _epilogue_args(bias, gate, M, N, device):

@@ -32,6 +32,7 @@ SIGNATURES = {
     "comp_gemm_workspace_bytes": (_i64, [_i64, _i64]),
     "comp_gemm_workspace_bytes_mnk": (_i64, [_i64, _i64, _i64]),
     "comp_gemm_f32x16_ws": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp]),
+    "comp_geglu_f32": (_int, [_vp, _vp, _vp, _i64, _vp]),
     "comp_gemm_f32x16_epilogue": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp]),
     "comp_gemm_f16x2_epilogue": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "comp_gemm_f32x16_noalloc": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),

@@ -216,6 +216,23 @@ comp_status_t comp_merge_f32(const float* acc_hi, const float* acc_lo, float* y,
     return launch_merge(acc_hi, acc_lo, y, n, dev, static_cast<cudaStream_t>(stream));
 }
 
+comp_status_t comp_geglu_f32(const float* gate, const float* up, float* out, int64_t n, comp_stream_t stream)
+{
+    if (n < 0 || n > INT64_MAX / 4)
+        return COMP_ERR_INVALID_VALUE;
+    if (n == 0)
+        return COMP_OK;
+    if (!gate || !up || !out)
+        return COMP_ERR_INVALID_VALUE;
+    if ((out != gate && overlap(out, 4 * n, gate, 4 * n)) || (out != up && overlap(out, 4 * n, up, 4 * n)))
+        return COMP_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    const comp_status_t st = current_device(&dev);
+    if (st != COMP_OK)
+        return st;
+    return launch_geglu(gate, up, out, n, dev, static_cast<cudaStream_t>(stream));
+}
+
 comp_status_t comp_gemm_f32x16_variant(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                        int variant, comp_stream_t stream)
 {
@@ -296,7 +313,17 @@ comp_status_t comp_gemm_f32x16_epilogue(const float* x, const uint16_t* W, const
 {
     if (!epilogue_args_ok(bias, gate, y, M, N))
         return COMP_ERR_INVALID_VALUE;
-    return gemm_ws_impl(x, W, y, M, N, K, workspace, workspace_bytes, stream, Epilogue{bias, gate});
+    // the bias in the product kernel's epilogue; the gate by the GEGLU dispatch
+    // on y in place right after, on the same stream (on GB300 the gate's erfc
+    // work stalls the tensor pipe when the product kernel does it)
+    comp_status_t st = gemm_ws_impl(x, W, y, M, N, K, workspace, workspace_bytes, stream, Epilogue{bias, nullptr});
+    if (st != COMP_OK || !gate || M == 0 || N == 0)
+        return st;
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != COMP_OK)
+        return st;
+    return launch_geglu(gate, y, y, M * N, dev, static_cast<cudaStream_t>(stream));
 }
 
 comp_status_t comp_gemm_f16x2_epilogue(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, const float* bias,

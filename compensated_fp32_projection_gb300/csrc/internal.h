@@ -26,6 +26,8 @@ comp_status_t launch_split_padded(const float* x, uint16_t* hi, uint16_t* lo, in
                                   const DeviceInfo& dev, cudaStream_t stream);
 comp_status_t launch_pad_rows(const uint16_t* src, uint16_t* dst, int64_t rows, int64_t K, int64_t Kp,
                               const DeviceInfo& dev, cudaStream_t stream);
+comp_status_t launch_geglu(const float* gate, const float* up, float* out, int64_t n, const DeviceInfo& dev,
+                           cudaStream_t stream);
 comp_status_t launch_merge(const float* acc_hi, const float* acc_lo, float* y, int64_t n, const DeviceInfo& dev,
                            cudaStream_t stream);
 comp_status_t launch_gemm_simt(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,

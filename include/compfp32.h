@@ -88,6 +88,20 @@ comp_status_t comp_split_f32(const float* x, uint16_t* hi, uint16_t* lo, int64_t
 comp_status_t comp_merge_f32(const float* acc_hi, const float* acc_lo, float* y, int64_t n, comp_stream_t stream);
 
 /*
+ * comp_geglu_f32 — the GEGLU step of the FP32 feed-forward layers as one
+ * dispatch (laya.cpp docs/vulkan.md, feed-forward paragraph: a fused GEGLU
+ * shader, with no separate gate copy, activation or multiplication
+ * dispatches):
+ *   out[i] = gelu(gate[i]) * up[i],  gelu(g) = g * Phi(g),
+ *   Phi(g) = erfc(-g / sqrt 2) / 2  (the exact GELU; CUDA's erfcf),
+ * each operation a binary32 operation rounded to nearest even.
+ *   gate, up : n binary32 values (input).   out : n binary32 values (output).
+ * out may be exactly gate or exactly up (in place); any other overlap is
+ * COMP_ERR_INVALID_VALUE, as are n < 0 and a NULL pointer with n > 0.
+ */
+comp_status_t comp_geglu_f32(const float* gate, const float* up, float* out, int64_t n, comp_stream_t stream);
+
+/*
  * comp_gemm_f32x16 — the fused compensated projection (laya.cpp docs/vulkan.md,
  * compensated-FP32 paragraph and the fused-build paragraph):
  *   y[m,n] = acc_hi[m,n] + acc_lo[m,n] * 2^-10, with acc_hi, acc_lo the FP32
@@ -208,7 +222,12 @@ comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, i
  *   out[m,n] = gelu(gate[m,n]) * (y[m,n] + bias[n]),
  *   gelu(g) = g * Phi(g), Phi(g) = erfc(-g / sqrt 2) / 2 (the exact GELU),
  * with y the compensated projection.  Each operation is an FP32 operation
- * rounded to nearest even; erfc is CUDA's erfcf.
+ * rounded to nearest even; erfc is CUDA's erfcf.  The bias is added in the
+ * product kernel's epilogue; the gate is applied right after on the same
+ * stream by comp_geglu_f32 on y in place (on GB300 the gate's erfc work
+ * stalls the tensor cores when the product kernel does it at tile ends).
+ * comp_gemm_f16x2_epilogue applies both inside the product kernel; the two
+ * give identical bits.
  *   bias : [N] binary32, or NULL for none (input).
  *   gate : [M, N] binary32 row-major, or NULL for a factor of 1 (input), e.g.
  *          the gate projection of the same x computed by an earlier call.

@@ -118,6 +118,16 @@ def test_epilogue_argument_errors(lib):
     assert e2(P(4096), P(1 << 16), P(1 << 20), None, None, P(y), 4, 8, 8, 4, None) == 1  # variant out of range
 
 
+def test_geglu_argument_errors(lib):
+    f = lib.comp_geglu_f32
+    # comp_geglu_f32(gate, up, out, n, stream)
+    assert f(P(4096), P(1 << 16), P(1 << 20), -1, None) == 1
+    assert f(None, P(1 << 16), P(1 << 20), 8, None) == 1
+    assert f(P(4096), P(1 << 16), P(4096 + 4), 8, None) == 1  # out partly overlaps gate
+    assert f(P(4096), P(1 << 16), P((1 << 16) + 4), 8, None) == 1  # out partly overlaps up
+    assert f(None, None, None, 0, None) == 0  # n = 0: no-op
+
+
 def test_workspace_bytes_mnk(lib):
     assert lib.comp_gemm_workspace_bytes_mnk(1000, 771, 1027) == 4 * 1000 * 1032 + 2 * 771 * 1032
     assert lib.comp_gemm_workspace_bytes_mnk(4096, 4096, 4096) == 4 * 4096 * 4096 + 2 * 4096 * 4096

@@ -1,7 +1,8 @@
-"""GPU parity of the GEGLU epilogue (laya.cpp docs/vulkan.md, feed-forward
-paragraph: gate activation and multiplication fused into the dispatch):
+"""GPU parity of the GEGLU step (laya.cpp docs/vulkan.md, feed-forward
+paragraph: gate activation and multiplication fused into one dispatch):
 out = gelu(gate) * (y + bias) applied by every product kernel to the merged
-projection, against the oracle's epilogue of the oracle's projection.
+projection, and by the streaming comp_geglu_f32 dispatch, against the
+oracle's epilogue of the oracle's projection.
 
 Tolerance per element: the projection's gate, 4e-6 * sum|x||w|, scaled by
 |gelu(g)|, plus the FP32 epilogue's own rounding, 2^-20 * (16 + g^2) relative
@@ -129,3 +130,58 @@ def test_epilogue_rejects_overlap_and_bad_shapes(pkg):
         pkg.comp_gemm_f32x16_epilogue(x, W, None, y, y=y)
     with pytest.raises(ValueError):
         pkg.comp_gemm_f32x16_epilogue(x, W, torch.zeros(15, device="cuda"))
+
+
+def _geglu_check(out, gate, up, orc):
+    g, u = gate.cpu().numpy(), up.cpu().numpy()
+    ref = orc.epilogue(u.reshape(1, -1), None, g.reshape(1, -1)).reshape(-1).astype(np.float64)
+    gel = np.abs(orc.epilogue(np.ones((1, g.size), np.float32), None, g.reshape(1, -1)).reshape(-1).astype(np.float64))
+    tol = 2.0**-20 * (16.0 + g.astype(np.float64) ** 2) * gel * np.abs(u.astype(np.float64)) + 1e-37
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= tol), f"max err/tol {float(np.max(err / tol))}"
+
+
+@pytest.mark.parametrize("n", [1, 7, 4096, 1_000_003])
+def test_geglu_dispatch(pkg, orc, n):
+    # the feed-forward paragraph's single GEGLU dispatch: out = gelu(gate) * up
+    g = torch.Generator().manual_seed(n)
+    gate = torch.randn(n, generator=g) * 2.5
+    up = torch.randn(n, generator=g) * 3.0
+    out = pkg.comp_geglu_f32(gate.cuda(), up.cuda())
+    _geglu_check(out, gate, up, orc)
+
+
+def test_geglu_in_place_and_misaligned(pkg, orc):
+    g = torch.Generator().manual_seed(4)
+    gate = torch.randn(10_001, generator=g) * 2.0
+    up = torch.randn(10_001, generator=g)
+    ref = pkg.comp_geglu_f32(gate.cuda(), up.cuda())
+    u2 = up.cuda()
+    pkg.comp_geglu_f32(gate.cuda(), u2, out=u2)  # out is up
+    g2 = gate.cuda()
+    pkg.comp_geglu_f32(g2, up.cuda(), out=g2)  # out is gate
+    assert torch.equal(u2.view(torch.int32), ref.view(torch.int32))
+    assert torch.equal(g2.view(torch.int32), ref.view(torch.int32))
+    # views starting one element in: 4-byte aligned only, the scalar kernel
+    gb, ub = gate.cuda(), up.cuda()
+    out = pkg.comp_geglu_f32(gb[1:], ub[1:])
+    assert torch.equal(out.view(torch.int32), ref[1:].view(torch.int32))
+    _geglu_check(ref, gate, up, orc)
+
+
+@pytest.mark.parametrize("shape", [(512, 8192, 256), (16, 4096, 512), (300, 520, 264)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_streaming_gate_equals_gate_in_the_product(pkg, shape):
+    # comp_gemm_f32x16_epilogue applies the gate with the GEGLU dispatch after
+    # the product; comp_gemm_f16x2_epilogue inside it: the same operations in
+    # the same order, so the same bits
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=3)
+    b, gate = operands(M, N, True, True, seed=9)
+    x, W, b, gate = x.cuda(), W.cuda(), b.cuda(), gate.cuda()
+    y1 = pkg.comp_gemm_f32x16_epilogue(x, W, b, gate)
+    hi, lo = pkg.comp_split_f32(x)
+    y2 = pkg.comp_gemm_f16x2_epilogue(hi, lo, W, b, gate)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
