@@ -114,7 +114,7 @@ def comp_gemm_f32x16(x, W, y=None, stream=None):
 
 def comp_gemm_f32x16_variant(x, W, variant, y=None, stream=None):
     """comp_gemm_f32x16 with a chosen kernel path (0 auto, 1 TMA loads, 2 plain loads,
-    3 operands swapped with the split fused, M <= 32)."""
+    3 operands swapped with the split fused, M <= 32, 4 CTA pairs with the split fused)."""
     M, N, K, y = _gemm_args(x, W, y)
     _native.call("comp_gemm_f32x16_variant", x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K, int(variant),
                  _stream(x, stream))

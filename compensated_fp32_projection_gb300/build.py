@@ -78,7 +78,7 @@ def _compile(src: str) -> tuple[str, str]:
 # launch register count; a different count could make setmaxnreg.inc wait
 # forever, so the build refuses it.
 SETMAXNREG_KERNELS = {"comp_gemm_kernel": 96, "comp_f16x2_kernel": 168, "comp_f16x2_pair_kernel": 168,
-                      "comp_f16x2_splitk_kernel": 168}
+                      "comp_f16x2_splitk_kernel": 168, "comp_f32x16_pair_kernel": 128}
 
 
 def _check_register_budget(ptxas_log: str) -> None:

@@ -236,11 +236,13 @@ comp_status_t comp_geglu_f32(const float* gate, const float* up, float* out, int
 comp_status_t comp_gemm_f32x16_variant(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                        int variant, comp_stream_t stream)
 {
-    if (variant < 0 || variant > 3)
+    if (variant < 0 || variant > 4)
         return COMP_ERR_INVALID_VALUE;
-    // the fused swapped-operand kernel: at most 32 rows, TMA-legal W and x
-    if (variant == 3 && (M > 32 || K % 8 != 0 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0 ||
-                         (reinterpret_cast<uintptr_t>(W) & 15u) != 0))
+    // the fused swapped-operand kernel (at most 32 rows) and the fused kernel
+    // on CTA pairs: TMA-legal W and x
+    const bool tma_legal = K % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+                           (reinterpret_cast<uintptr_t>(W) & 15u) == 0;
+    if ((variant == 3 && (M > 32 || !tma_legal)) || (variant == 4 && !tma_legal))
         return COMP_ERR_INVALID_VALUE;
     DeviceInfo dev;
     bool empty;

@@ -1163,6 +1163,277 @@ constexpr uint32_t kFaultPairMma = 0x702;
 constexpr uint32_t kFaultPairPromote = 0x703;
 
 
+// Bounded wait on a barrier that the other CTA of the cluster arrives on after
+// a shared-memory release fence at cluster scope: relaxed polls at cluster
+// scope, then the matching acquire fence.
+__device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t parity, int* abort_flag, uint32_t code)
+{
+    const long long start = clock64();
+    while (!mbar_try_wait_relaxed_cluster(bar, parity)) {
+        if (*reinterpret_cast<volatile int*>(abort_flag))
+            return false;
+        if (clock64() - start > kWaitLimit) {
+            atomicCAS(&g_fault_word, 0u, code);
+            *reinterpret_cast<volatile int*>(abort_flag) = 1;
+            return false;
+        }
+    }
+    fence_acquire_smem_cluster();
+    return true;
+}
+
+// Descriptor offset, in 16-byte units from the stage base, of K slice j
+// (16 of K) of the hi or lo operand of a stage.  Planes: the hi box (128 rows
+// of 64 FP16, 128 bytes each), then the lo box.  Fused kernel:
+// line r of box h (h = 0, 1) holds the hi values of K 32h .. 32h+31 of row r
+// in its first 64 bytes and their lo values in its last 64 bytes.  Both are
+// 128-byte rows with the 128-byte swizzle, so one descriptor form serves.
+template <bool FUSED>
+__device__ __forceinline__ constexpr uint32_t a_slice(int j, bool lo)
+{
+    return FUSED ? static_cast<uint32_t>((j >> 1) * (pair::kPlaneBytes >> 4) + (lo ? 4 : 0) + 2 * (j & 1))
+                 : static_cast<uint32_t>((lo ? (pair::kPlaneBytes >> 4) : 0) + 2 * j);
+}
+
+// The MMA issuer of a CTA pair (leader CTA, the whole warp runs the loop,
+// lane 0 waits and issues), one chunk of CH K blocks at a time: lo * W^T of
+// the chunk into a fresh accumulator, then hi * W^T, whose first MMA scales
+// the accumulator by 2^-10 on input.  Stage s holds, in both CTAs, the hi and
+// lo values of the CTA's 128 rows (first 32 KB, laid out as a_slice<FUSED>
+// says) and the CTA's half of the W rows.
+//   Two-pass product: bars->full[s] (leader) completes when all of them have
+// landed; a chunk starts once all its stages are in.
+//   Fused kernel: bars->full[s] counts the W bytes and split[s] the split
+// warps of both CTAs (the other CTA's after a shared-memory release at
+// cluster scope: relaxed polls at cluster scope, then the acquire fence).  A
+// chunk starts once its first stage is ready, and each later stage is waited
+// for just before its first MMA, so the products of a stage overlap the split
+// of the next.
+template <int BN, int NS, int CH, bool FUSED>
+__device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint64_t* split, uint8_t* smem, uint32_t tmem,
+                                              int total, const Problem& P, int lane)
+{
+    using C = pair::Cfg<BN, NS, CH>;
+    const uint32_t leader = lane == 0 ? 1u : 0u;
+    const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
+    auto test_stage = [&](int g) -> bool {
+        const int s = g % NS;
+        const uint32_t par = (g / NS) & 1;
+        if constexpr (FUSED) {
+            if (!(mbar_test_wait(&bars->full[s], par) && mbar_test_wait_relaxed_cluster(&split[s], par)))
+                return false;
+            fence_acquire_smem_cluster();
+            return true;
+        } else {
+            return mbar_test_wait(&bars->full[s], par);
+        }
+    };
+    auto wait_stage = [&](int g) -> bool {  // lane 0
+        const int s = g % NS;
+        const uint32_t par = (g / NS) & 1;
+        bool ok = wait_bounded(&bars->full[s], par, &bars->abort, kFaultPairMma);
+        if constexpr (FUSED)
+            ok = ok && wait_bounded_cluster(&split[s], par, &bars->abort, kFaultPairMma);
+        return ok;
+    };
+    constexpr int kFirst = FUSED ? 1 : CH;  // stages a chunk waits for before its first MMA
+    auto test_chunk = [&](int g, int c, int n) -> bool {
+        bool r = c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1);
+#pragma unroll
+        for (int i = 0; i < kFirst; ++i)
+            if (i < n)
+                r = r && test_stage(g + i);
+        return r;
+    };
+    auto wait_chunk = [&](int g, int c, int n) -> bool {
+        bool ok = true;
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < kFirst; ++i)
+                if (ok && i < n)
+                    ok = wait_stage(g + i);
+            if (ok && c >= 2)
+                ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort, kFaultPairMma);
+        }
+        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    };
+    int g = 0, c = 0, kb = 0;
+    int n = (P.nk < CH) ? P.nk : CH;
+    bool ok = total == 0 || wait_chunk(0, 0, n);
+    while (g < total && ok) {
+        const int b = c & 1;
+        tc_fence_after();
+        const uint32_t d = tmem + b * BN;
+        auto sdesc = [&](int blk, uint32_t off) {
+            return desc0 + static_cast<uint64_t>(((blk % NS) * C::kStageBytes + off) >> 4);
+        };
+        for (int i = 0; i < n; ++i) {  // lo * W^T of the chunk; the very first overwrites D
+            if (FUSED && i >= kFirst) {
+                bool r = true;
+                if (lane == 0)
+                    r = test_stage(g + i) || wait_stage(g + i);
+                ok = __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+                if (!ok)
+                    break;
+                tc_fence_after();
+            }
+            const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * pair::kPlaneBytes);
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j)
+                umma_f16_pair_by(leader, d, a + a_slice<FUSED>(j, true), w + 2 * j, C::kIdesc,
+                                 (i > 0 || j > 0) ? 1u : 0u);
+        }
+        if (!ok)
+            break;
+        const int g2 = g + n, c2 = c + 1;
+        const int kb2 = (kb + n == P.nk) ? 0 : kb + n;
+        const int n2 = (P.nk - kb2 < CH) ? P.nk - kb2 : CH;
+        bool ready2 = true;
+        for (int i = 0; i < n; ++i) {  // hi * W^T; the first scales D by 2^-10 on input
+            const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * pair::kPlaneBytes);
+            if (i == n - 1 && g2 < total)
+                ready2 = test_chunk(g2, c2, n2);
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j) {
+                if (i == 0 && j == 0)
+                    umma_f16_pair_scale10_by(leader, d, a + a_slice<FUSED>(0, false), w, C::kIdesc);
+                else
+                    umma_f16_pair_by(leader, d, a + a_slice<FUSED>(j, false), w + 2 * j, C::kIdesc, 1u);
+            }
+            umma_commit_pair_by(leader, &bars->empty[(g + i) % NS], 0x3);
+        }
+        umma_commit_pair_by(leader, &bars->dfull[b], 0x3);
+        g = g2;
+        c = c2;
+        kb = kb2;
+        n = n2;
+        if (g < total && !ready2)
+            ok = wait_chunk(g, c, n);
+    }
+    if (!ok) {
+        umma_commit_pair_by(leader, &bars->drain, 0x1);
+        if (lane == 0)
+            drain_wait(&bars->drain, 0);
+        __syncwarp();
+    }
+}
+
+// Promotion in both CTAs of a pair (warps 4 .. 4 + kPromoters - 1): R += D per
+// chunk in FP32 registers, RT accumulator columns per tensor-memory round
+// trip; at the tile end the optional epilogue, then y.  Warp w owns TMEM lane
+// quarter w % 4 (32 rows of the CTA's 128) and one column half of the tile.
+template <int BN, int NS, int CH, bool EPI, int RT>
+__device__ __forceinline__ void pair_promote_role(pair::Barriers* bars, const CUtensorMap* tmap_y, uint8_t* ystage,
+                                                  uint32_t tmem, int total, const Problem& P, uint32_t rank,
+                                                  int pair_id, int num_pairs, int warp, int lane)
+{
+    using C = pair::Cfg<BN, NS, CH>;
+    static_assert(RT % 16 == 0 && RT <= 64, "round trip");
+    const int wq = warp & 3;         // TMEM lane quarter
+    const int wh = (warp - 4) >> 2;  // column half of the tile
+    const uint32_t dfree0 = mapa_shared(&bars->dfree[0], 0);  // the leader's dfree barriers
+    float R[C::kHalf];
+#pragma unroll
+    for (int i = 0; i < C::kHalf; ++i)
+        R[i] = 0.0f;
+    int g = 0, c = 0, kb = 0;
+    int t = pair_id;
+    uint8_t* ybuf = ystage + (warp - 4) * (2 * pair::kYPiece);
+    int ng = 0;  // y pieces stored by this warp (its bulk groups, alternating buffers)
+    while (g < total) {
+        const int n = (P.nk - kb < CH) ? P.nk - kb : CH;
+        const int b = c & 1;
+        // one warp polls the barrier; the others wait at a named barrier
+        if (warp == 4)
+            (void)lane0_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultPairPromote);
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * pair::kPromoters) : "memory");
+        if (*reinterpret_cast<volatile int*>(&bars->abort))
+            break;
+        tc_fence_after();
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * BN + wh * C::kHalf;
+#pragma unroll
+        for (int c0 = 0; c0 < C::kHalf; c0 += RT) {  // RT columns per round trip
+            uint32_t v[RT];
+#pragma unroll
+            for (int q = 0; q < RT / 16; ++q)
+                if (c0 + 16 * q < C::kHalf)
+                    tmem_ld16(taddr + c0 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < RT; i += 2)
+                if (c0 + i < C::kHalf)
+                    add2(R[c0 + i], R[c0 + i + 1], v[i], v[i + 1]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive_cluster(dfree0 + static_cast<uint32_t>(b) * 8u);
+        g += n;
+        ++c;
+        kb += n;
+        if (kb == P.nk) {
+            // tile finished: R holds y[m, nb .. nb + BN/2) for this thread's row m
+            const int64_t row0 = static_cast<int64_t>(tile_m(t, P)) * pair::kRows + rank * BM + wq * 32;
+            const int64_t m = row0 + lane;
+            const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
+            if constexpr (EPI) {
+                static_assert(C::kHalf % 16 == 0, "epilogue in pieces of 16 columns");
+                if (m < P.M) {
+#pragma unroll
+                    for (int p = 0; p < C::kHalf; p += 16)
+                        epilogue16(R + p, m, nb + p, P);
+                }
+            }
+            if (P.tma_y) {
+                // 16-column pieces through shared memory; the tensor-map store
+                // clips rows >= M and columns >= N
+#pragma unroll
+                for (int p = 0; p < C::kHalf / 16; ++p) {
+                    if (row0 >= P.M || nb + 16 * p >= P.N)
+                        continue;
+                    uint8_t* buf = ybuf + (ng & 1) * pair::kYPiece;
+                    if (ng >= 2) {  // the store that last read this buffer has finished reading it
+                        if (lane == 0)
+                            bulk_wait_group_read1();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)  // 64-byte swizzle: 16-byte chunk j of row `lane`
+                        st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), R[16 * p + 4 * j],
+                                     R[16 * p + 4 * j + 1], R[16 * p + 4 * j + 2], R[16 * p + 4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(tmap_y, buf, static_cast<int32_t>(nb + 16 * p), static_cast<int32_t>(row0));
+                        bulk_commit_group();
+                    }
+                    ++ng;
+                }
+            } else if (m < P.M) {
+                float* yrow = P.y + m * P.N;
+                if (P.vec_y && nb + C::kHalf <= P.N) {
+#pragma unroll
+                    for (int i = 0; i < C::kHalf; i += 4)
+                        *reinterpret_cast<float4*>(yrow + nb + i) = make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < C::kHalf; ++i)
+                        if (nb + i < P.N)
+                            yrow[nb + i] = R[i];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < C::kHalf; ++i)
+                R[i] = 0.0f;
+            kb = 0;
+            t += num_pairs;
+        }
+    }
+    if (lane == 0)
+        bulk_wait_group0();  // y stores complete
+    __syncwarp();
+}
+
 template <int BN, int NS, int CH, bool EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     comp_f16x2_pair_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
@@ -1256,185 +1527,237 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                 }
             }
         } else if (warp == 1 && leader_cta) {
-            // ---------------- MMA issuer (leader CTA), one chunk of CH K blocks at a time ----------------
-            const uint32_t leader = lane == 0 ? 1u : 0u;
-            const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
-            auto test_chunk = [&](int g, int c, int n) -> bool {
-                bool r = c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1);
-#pragma unroll
-                for (int i = 0; i < CH; ++i)
-                    if (i < n)
-                        r = mbar_test_wait(&bars->full[(g + i) % NS], ((g + i) / NS) & 1) && r;
-                return r;
-            };
-            auto wait_chunk = [&](int g, int c, int n) -> bool {
-                bool ok = true;
-                if (lane == 0) {
-#pragma unroll
-                    for (int i = 0; i < CH; ++i)
-                        if (ok && i < n)
-                            ok = wait_bounded(&bars->full[(g + i) % NS], ((g + i) / NS) & 1, &bars->abort,
-                                                      kFaultPairMma);
-                    if (ok && c >= 2)
-                        ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort,
-                                                  kFaultPairMma);
-                }
-                return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            };
-            int g = 0, c = 0, kb = 0;
-            int n = (P.nk < CH) ? P.nk : CH;
-            bool ok = total == 0 || wait_chunk(0, 0, n);
-            while (g < total && ok) {
-                const int b = c & 1;
-                tc_fence_after();
-                const uint32_t d = tmem + b * BN;
-                auto sdesc = [&](int blk, uint32_t off) {
-                    return desc0 + static_cast<uint64_t>(((blk % NS) * C::kStageBytes + off) >> 4);
-                };
-                for (int i = 0; i < n; ++i) {  // lo * W^T of the chunk; the very first overwrites D
-                    const uint64_t a = sdesc(g + i, pair::kPlaneBytes), w = sdesc(g + i, 2 * pair::kPlaneBytes);
-#pragma unroll
-                    for (int j = 0; j < BK / 16; ++j)
-                        umma_f16_pair_by(leader, d, a + 2 * j, w + 2 * j, C::kIdesc, (i > 0 || j > 0) ? 1u : 0u);
-                }
-                const int g2 = g + n, c2 = c + 1;
-                const int kb2 = (kb + n == P.nk) ? 0 : kb + n;
-                const int n2 = (P.nk - kb2 < CH) ? P.nk - kb2 : CH;
-                bool ready2 = true;
-                for (int i = 0; i < n; ++i) {  // hi * W^T; the first scales D by 2^-10 on input
-                    const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * pair::kPlaneBytes);
-                    if (i == n - 1 && g2 < total)
-                        ready2 = test_chunk(g2, c2, n2);
-#pragma unroll
-                    for (int j = 0; j < BK / 16; ++j) {
-                        if (i == 0 && j == 0)
-                            umma_f16_pair_scale10_by(leader, d, a, w, C::kIdesc);
-                        else
-                            umma_f16_pair_by(leader, d, a + 2 * j, w + 2 * j, C::kIdesc, 1u);
-                    }
-                    umma_commit_pair_by(leader, &bars->empty[(g + i) % NS], 0x3);
-                }
-                umma_commit_pair_by(leader, &bars->dfull[b], 0x3);
-                g = g2;
-                c = c2;
-                kb = kb2;
-                n = n2;
-                if (g < total && !ready2)
-                    ok = wait_chunk(g, c, n);
-            }
-            if (!ok) {
-                umma_commit_pair_by(leader, &bars->drain, 0x1);
-                if (lane == 0)
-                    drain_wait(&bars->drain, 0);
-                __syncwarp();
-            }
+            // ---------------- MMA issuer (leader CTA) ----------------
+            pair_mma_role<BN, NS, CH, false>(bars, nullptr, smem, tmem, total, P, lane);
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(pair::kPromoRegs));
         // ---------------- promotion (both CTAs): R += D per chunk, then store y ----------------
-        const int wq = warp & 3;         // TMEM lane quarter
-        const int wh = (warp - 4) >> 2;  // column half of the tile
-        const uint32_t dfree0 = mapa_shared(&bars->dfree[0], 0);  // the leader's dfree barriers
-        float R[C::kHalf];
+        pair_promote_role<BN, NS, CH, EPI, 64>(bars, &tmap_y, ystage, tmem, total, P, rank, pair_id, num_pairs, warp,
+                                               lane);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still signal its barriers
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The fused projection on CTA pairs (comp_gemm_f32x16 for outputs of about a
+// wave of 256-row tiles or more): the pair product above, reading FP32 x
+// instead of the split planes, so nothing but y leaves the kernel.
+//
+// Each CTA's producer loads its 128 rows of the K block of x by TMA, as two
+// 128 x 32 FP32 boxes with the 128-byte swizzle, into the 32 KB of the stage
+// where the pair product keeps its hi and lo boxes (the FP32 block has exactly
+// their size).  Four split warps, one thread per row, then split each
+// 128-byte line in place with the arithmetic of comp_split_f32: line r of box
+// h holds x[r, 32h .. 32h+31]; afterwards its first 64 bytes hold their hi
+// values and its last 64 bytes their lo values.  A line is read whole before
+// it is written, and no line depends on another, so a thread orders only its
+// own accesses.  The MMA reads hi and lo K slices at their offsets within the
+// same 128-byte swizzled rows (a_slice<true>), in the order of the pair
+// product, so both forms give identical bits.
+//
+// Signalling.  The TMA bytes of x count on a barrier of the CTA that loads
+// them (xfull), which its split warps wait on.  A stage is ready for the MMA,
+// issued by the leader CTA, when both CTAs' W halves have landed (bytes on
+// the leader's `full`) and all eight split warps have written hi and lo
+// (sfull).  The split warps publish their generic-proxy writes to the tensor
+// cores with fence.proxy.async; the leader's split warps arrive on the
+// leader's sfull, the other CTA's after a release fence at cluster scope
+// restricted to shared memory, with a relaxed arrival.  The MMA lane polls
+// sfull relaxed at cluster scope and then takes the matching acquire fence.
+// ---------------------------------------------------------------------------
+namespace fpair {
+constexpr int kSplitters = 4;  // warps 12-15: split x in place, one thread per row
+constexpr int kThreads = 128 + 32 * (pair::kPromoters + kSplitters);
+// 512 threads launch with 128 registers each (pool 65536): control 40,
+// promotion 208, split 56: 128*40 + 256*208 + 128*56 = 65536.  The build
+// checks the 128.
+constexpr int kLaunchRegs = 128;
+constexpr int kCtrlRegs = 40;
+constexpr int kPromoRegs = 208;
+constexpr int kSplitRegs = 56;
+static_assert(128 * kCtrlRegs + 32 * pair::kPromoters * kPromoRegs + 32 * kSplitters * kSplitRegs <=
+                  kThreads * kLaunchRegs,
+              "register split");
+constexpr int kRoundTrip = 32;  // accumulator columns per tensor-memory round trip (fits 208 registers)
+
+struct Barriers : pair::Barriers {
+    uint64_t xfull[pair::kMaxStages];  // this CTA's FP32 x boxes landed (TMA bytes)
+    uint64_t sfull[pair::kMaxStages];  // leader: the split warps of both CTAs wrote hi and lo
+};
+}  // namespace fpair
+
+// Fault codes of the fused CTA-pair kernel (its MMA and promotion roles report
+// the pair product's codes).
+constexpr uint32_t kFaultFpairProducer = 0x901;
+constexpr uint32_t kFaultFpairSplit = 0x903;
+
+__device__ __forceinline__ void sts128(uint32_t addr, const uint32_t (&v)[4])
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
+
+// Splits 8 consecutive values (two 16-byte chunks a, b of x) into one 16-byte
+// chunk of hi and one of lo.
+__device__ __forceinline__ void split8(const float4& a, const float4& b, uint32_t (&h)[4], uint32_t (&l)[4])
+{
+    split2(a.x, a.y, h[0], l[0]);
+    split2(a.z, a.w, h[1], l[1]);
+    split2(b.x, b.y, h[2], l[2]);
+    split2(b.z, b.w, h[3], l[3]);
+}
+
+// One 128-byte line of a stage (32 FP32 values of a row, 16-byte chunk c at
+// (c ^ sw) << 4) split in place: hi of the 32 values into chunks 0..3, lo
+// into chunks 4..7.  All eight chunks are read before the first write.
+__device__ __forceinline__ void split_line_in_place(uint32_t line, uint32_t sw)
+{
+    float4 v[8];
 #pragma unroll
-        for (int i = 0; i < C::kHalf; ++i)
-            R[i] = 0.0f;
-        int g = 0, c = 0, kb = 0;
-        int t = pair_id;
-        uint8_t* ybuf = ystage + (warp - 4) * (2 * pair::kYPiece);
-        int ng = 0;  // y pieces stored by this warp (its bulk groups, alternating buffers)
-        while (g < total) {
-            const int n = (P.nk - kb < CH) ? P.nk - kb : CH;
-            const int b = c & 1;
-            // one warp polls the barrier; the others wait at a named barrier
-            if (warp == 4)
-                (void)lane0_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultPairPromote);
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * pair::kPromoters) : "memory");
-            if (*reinterpret_cast<volatile int*>(&bars->abort))
-                break;
-            tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * BN + wh * C::kHalf;
+    for (uint32_t c = 0; c < 8; ++c)
+        v[c] = lds128(line + ((c ^ sw) << 4));
 #pragma unroll
-            for (int c0 = 0; c0 < C::kHalf; c0 += 64) {  // up to 64 columns per round trip
-                uint32_t v[64];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (c0 + 16 * q < C::kHalf)
-                        tmem_ld16(taddr + c0 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 64; i += 2)
-                    if (c0 + i < C::kHalf)
-                        add2(R[c0 + i], R[c0 + i + 1], v[i], v[i + 1]);
+    for (uint32_t c = 0; c < 4; ++c) {  // values 8c .. 8c+7
+        uint32_t h[4], l[4];
+        split8(v[2 * c], v[2 * c + 1], h, l);
+        sts128(line + ((c ^ sw) << 4), h);
+        sts128(line + (((4 + c) ^ sw) << 4), l);
+    }
+}
+
+template <int BN, int NS, int CH, bool EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fpair::kThreads, 1)
+    comp_f32x16_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                            const __grid_constant__ CUtensorMap tmap_y, const Problem P)
+{
+    using C = pair::Cfg<BN, NS, CH>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    fpair::Barriers* bars = reinterpret_cast<fpair::Barriers*>(smem + NS * C::kStageBytes);
+    static_assert(sizeof(fpair::Barriers) <= pair::kBarBytes, "barrier area");
+    uint8_t* ystage = smem + NS * C::kStageBytes + pair::kBarBytes;  // 1024-aligned
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader_cta = rank == 0;
+    const int pair_id = static_cast<int>(blockIdx.x >> 1);
+    const int num_pairs = static_cast<int>(gridDim.x >> 1);
+    const int num_tiles = P.tiles_m * P.tiles_n;  // pair tiles of 256 x BN
+    const int my_tiles = pair_id < num_tiles ? (num_tiles - 1 - pair_id) / num_pairs + 1 : 0;
+    const int total = my_tiles * P.nk;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bars->full[s], 1);  // leader: W bytes of both CTAs
+            mbar_init(&bars->empty[s], 1);
+            mbar_init(&bars->xfull[s], 1);
+            mbar_init(&bars->sfull[s], 2 * fpair::kSplitters);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->dfull[b], 1);
+            mbar_init(&bars->dfree[b], 2 * pair::kPromoters);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tmap_x);
+        tma_prefetch_desc(&tmap_w);
+        if (P.tma_y)
+            tma_prefetch_desc(&tmap_y);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&bars->tmem_base, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised before any remote arrival
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(fpair::kCtrlRegs));
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer (both CTAs): own 128 rows of x, own half of W ----------------
+            grid_dependency_wait();  // x may come from the previous kernel of the stream
+            const uint32_t full0 = mapa_shared(&bars->full[0], 0);  // the leader's W barriers
+            int issued = 0;
+            int t = pair_id, kb = 0;
+            for (int g = 0; g < total; ++g) {
+                const int s = g % NS;
+                if (g >= NS && !wait_bounded(&bars->empty[s], ((g / NS) - 1) & 1, &bars->abort, kFaultFpairProducer))
+                    break;
+                const int m0 = tile_m(t, P) * pair::kRows + static_cast<int>(rank) * BM;
+                const int n0 = tile_n(t, P) * BN + static_cast<int>(rank) * (BN / 2);
+                const int k0 = kb * BK;
+                uint8_t* st = smem + s * C::kStageBytes;
+                mbar_arrive_expect_tx(&bars->xfull[s], 2 * pair::kPlaneBytes);
+                tma_load_2d(st, &tmap_x, &bars->xfull[s], k0, m0);
+                tma_load_2d(st + pair::kPlaneBytes, &tmap_x, &bars->xfull[s], k0 + 32, m0);
+                if (leader_cta)
+                    mbar_arrive_expect_tx(&bars->full[s], 2 * C::kWBytes);
+                tma_load_2d_pair(st + 2 * pair::kPlaneBytes, &tmap_w, full0 + static_cast<uint32_t>(s) * 8u, k0, n0);
+                issued = g + 1;
+                if (++kb == P.nk) {
+                    kb = 0;
+                    t += num_pairs;
+                }
             }
-            tc_fence_before();
+            if (*reinterpret_cast<volatile int*>(&bars->abort)) {
+                for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
+                    drain_wait(&bars->xfull[g % NS], (g / NS) & 1);
+                if (leader_cta) {
+                    // the leader's W barriers count both CTAs' W loads
+                    for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
+                        drain_wait(&bars->full[g % NS], (g / NS) & 1);
+                } else {
+                    // this CTA's W loads complete on the leader's barriers: give them time to land
+                    const long long start = clock64();
+                    while (clock64() - start < (1ll << 22)) {
+                    }
+                }
+            }
+        } else if (warp == 1 && leader_cta) {
+            // ---------------- MMA issuer (leader CTA) ----------------
+            pair_mma_role<BN, NS, CH, true>(bars, bars->sfull, smem, tmem, total, P, lane);
+        }
+    } else if (warp < 4 + pair::kPromoters) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(fpair::kPromoRegs));
+        // ---------------- promotion (both CTAs): R += D per chunk, then store y ----------------
+        pair_promote_role<BN, NS, CH, EPI, fpair::kRoundTrip>(bars, &tmap_y, ystage, tmem, total, P, rank, pair_id,
+                                                              num_pairs, warp, lane);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(fpair::kSplitRegs));
+        // ---------------- split (both CTAs): each stage's x rows -> hi and lo in place ----------------
+        const uint32_t row = static_cast<uint32_t>(warp - 4 - pair::kPromoters) * 32u + lane;
+        const uint32_t sfull0 = mapa_shared(&bars->sfull[0], 0);  // the leader's split barriers
+        const uint32_t smem_s = smem_u32(smem);
+        for (int g = 0; g < total; ++g) {
+            const int s = g % NS;
+            if (!warp_wait(&bars->xfull[s], (g / NS) & 1, &bars->abort, kFaultFpairSplit))
+                break;
+            const uint32_t line = smem_s + static_cast<uint32_t>(s) * C::kStageBytes + row * 128u;
+            split_line_in_place(line, row & 7u);                       // K 0 .. 31 of the row
+            split_line_in_place(line + pair::kPlaneBytes, row & 7u);  // K 32 .. 63
+            fence_proxy_async_smem();  // generic-proxy stores, read next by the tensor cores
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive_cluster(dfree0 + static_cast<uint32_t>(b) * 8u);
-            g += n;
-            ++c;
-            kb += n;
-            if (kb == P.nk) {
-                // tile finished: R holds y[m, nb .. nb + BN/2) for this thread's row m
-                const int64_t row0 = static_cast<int64_t>(tile_m(t, P)) * pair::kRows + rank * BM + wq * 32;
-                const int64_t m = row0 + lane;
-                const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
-                if constexpr (EPI) {
-                    static_assert(C::kHalf % 16 == 0, "epilogue in pieces of 16 columns");
-                    if (m < P.M) {
-#pragma unroll
-                        for (int p = 0; p < C::kHalf; p += 16)
-                            epilogue16(R + p, m, nb + p, P);
-                    }
-                }
-                if (P.tma_y) {
-                    // 16-column pieces through shared memory; the tensor-map store
-                    // clips rows >= M and columns >= N
-#pragma unroll
-                    for (int p = 0; p < C::kHalf / 16; ++p) {
-                        if (row0 >= P.M || nb + 16 * p >= P.N)
-                            continue;
-                        uint8_t* buf = ybuf + (ng & 1) * pair::kYPiece;
-                        if (ng >= 2) {  // the store that last read this buffer has finished reading it
-                            if (lane == 0)
-                                bulk_wait_group_read1();
-                            __syncwarp();
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)  // 64-byte swizzle: 16-byte chunk j of row `lane`
-                            st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), R[16 * p + 4 * j],
-                                         R[16 * p + 4 * j + 1], R[16 * p + 4 * j + 2], R[16 * p + 4 * j + 3]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmap_y, buf, static_cast<int32_t>(nb + 16 * p), static_cast<int32_t>(row0));
-                            bulk_commit_group();
-                        }
-                        ++ng;
-                    }
-                } else if (m < P.M) {
-                    float* yrow = P.y + m * P.N;
-                    if (P.vec_y && nb + C::kHalf <= P.N) {
-#pragma unroll
-                        for (int i = 0; i < C::kHalf; i += 4)
-                            *reinterpret_cast<float4*>(yrow + nb + i) = make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < C::kHalf; ++i)
-                            if (nb + i < P.N)
-                                yrow[nb + i] = R[i];
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < C::kHalf; ++i)
-                    R[i] = 0.0f;
-                kb = 0;
-                t += num_pairs;
+            if (lane == 0) {
+                if (leader_cta)
+                    mbar_arrive(&bars->sfull[s]);
+                else
+                    mbar_arrive_release_smem_cluster(sfull0 + static_cast<uint32_t>(s) * 8u);
             }
         }
-        if (lane == 0)
-            bulk_wait_group0();  // y stores complete
-        __syncwarp();
     }
 
     tc_fence_before();
@@ -1872,6 +2195,13 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
             return COMP_ERR_INVALID_VALUE;
         return launch_swap_fused(x, W, y, M, N, K, dev, stream, epi);
     }
+    // more than 128 rows and about a wave of pair tiles: the fused kernel on
+    // CTA pairs (variant 4, or automatically with TMA-legal operands)
+    if (variant == 4 || (variant == 0 && fused_pair_preferred(x, W, M, N, K, dev))) {
+        if (!vec_ok)
+            return COMP_ERR_INVALID_VALUE;
+        return launch_fused_pair(x, W, y, M, N, K, dev, stream, epi);
+    }
     if (variant == 1 && !vec_ok)
         return COMP_ERR_INVALID_VALUE;
     bool use_vec = variant == 2 ? false : vec_ok;
@@ -2089,6 +2419,52 @@ comp_status_t launch_pair_bn(const CUtensorMap& th, const CUtensorMap& tl, const
                               : launch_pair_bn_t<BN, NS, CH, false>(th, tl, tw, ty, P, dev, stream);
 }
 
+template <int BN, int NS, int CH, bool EPI>
+comp_status_t launch_fpair_bn_t(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const Problem& P,
+                                const DeviceInfo& dev, cudaStream_t stream)
+{
+    using C = pair::Cfg<BN, NS, CH>;
+    static std::mutex mu;
+    static int pairs[64] = {};  // co-resident CTA pairs per device, 0 = not yet known
+    int np;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev.device < 0 || dev.device >= 64)
+            return COMP_ERR_CUDA;
+        if (pairs[dev.device] == 0) {
+            if (cudaFuncSetAttribute(comp_f32x16_pair_kernel<BN, NS, CH, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(C::kSmem)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return COMP_ERR_CUDA;
+            }
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count & ~1), 1, 1);
+            cfg.blockDim = dim3(fpair::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = C::kSmem;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, comp_f32x16_pair_kernel<BN, NS, CH, EPI>, &cfg) !=
+                    cudaSuccess ||
+                clusters <= 0) {
+                (void)cudaGetLastError();
+                clusters = dev.sm_count / 2;
+            }
+            pairs[dev.device] = clusters;
+        }
+        np = pairs[dev.device];
+    }
+    const int tiles = P.tiles_m * P.tiles_n;
+    const int grid = 2 * (tiles < np ? tiles : np);
+    return launch_pdl(comp_f32x16_pair_kernel<BN, NS, CH, EPI>, grid, fpair::kThreads, C::kSmem, stream, tx, tw, ty, P);
+}
+
+template <int BN, int NS, int CH>
+comp_status_t launch_fpair_bn(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const Problem& P,
+                              const DeviceInfo& dev, cudaStream_t stream)
+{
+    return (P.bias || P.gate) ? launch_fpair_bn_t<BN, NS, CH, true>(tx, tw, ty, P, dev, stream)
+                              : launch_fpair_bn_t<BN, NS, CH, false>(tx, tw, ty, P, dev, stream);
+}
+
 // N tile width for the two-pass product (tiles are all tensor work there).
 int pick_bn_x2(int64_t M, int64_t N, int sms)
 {
@@ -2281,6 +2657,48 @@ comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int
     // a stage larger: 4 x 48 KB (Mp 16), 3 x 64 KB (Mp 32)
     return mp == 16 ? launch_swap<16, 2, 4, true>(tx, none, tw, P, dev, stream)
                     : launch_swap<32, 2, 3, true>(tx, none, tw, P, dev, stream);
+}
+
+bool fused_pair_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K, const DeviceInfo& dev)
+{
+    // CTA pairs once the output fills about one wave of 128 x 192 tiles (the
+    // two-pass product's rule), TMA-legal operands
+    return M > BM && M * N >= static_cast<int64_t>(dev.sm_count) * BM * 192 && K % 8 == 0 && aligned16(x) &&
+           aligned16(W);
+}
+
+comp_status_t launch_fused_pair(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                                const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi)
+{
+    if (K % 8 != 0 || !aligned16(x) || !aligned16(W))
+        return COMP_ERR_INVALID_VALUE;
+    Problem P;
+    P.x = x;
+    P.W = W;
+    P.y = y;
+    P.M = static_cast<int>(M);
+    P.N = static_cast<int>(N);
+    P.K = static_cast<int>(K);
+    P.nk = static_cast<int>((K + BK - 1) / BK);
+    P.vec_y = (N % 4 == 0) && aligned16(y);
+    P.tma_y = 0;
+    P.bias = epi.bias;
+    P.gate = epi.gate;
+    // the pair product's tile width, so that both forms give identical bits
+    const int bn = pick_bn_pair(M, N, dev.sm_count / 2);
+    P.tiles_m = static_cast<int>((M + pair::kRows - 1) / pair::kRows);
+    P.tiles_n = static_cast<int>((N + bn - 1) / bn);
+    if (static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
+        return COMP_ERR_INVALID_VALUE;
+    CUtensorMap tx{}, tw{}, ty{};
+    // FP32 x as two 128 x 32 boxes per K block (128 bytes of a row each)
+    if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, K, M, 32, BM) ||
+        !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn / 2)))
+        return COMP_ERR_CUDA;
+    if (P.vec_y)
+        P.tma_y = encode_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, N, M, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+    return bn == 224 ? launch_fpair_bn<224, 4, 2>(tx, tw, ty, P, dev, stream)
+                     : launch_fpair_bn<256, 4, 2>(tx, tw, ty, P, dev, stream);
 }
 
 namespace {

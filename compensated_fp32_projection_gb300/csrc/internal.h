@@ -32,7 +32,6 @@ comp_status_t launch_merge(const float* acc_hi, const float* acc_lo, float* y, i
                            cudaStream_t stream);
 comp_status_t launch_gemm_simt(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                const DeviceInfo& dev, cudaStream_t stream);
-// variant: 0 automatic, 1 TMA loads, 2 plain loads.
 // Optional FP32 operations on the merged projection in the product kernels'
 // epilogue (GEGLU feed-forward step): y = gelu(gate) * (y + bias).
 struct Epilogue {
@@ -45,6 +44,15 @@ struct Epilogue {
 bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K);
 comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                 const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi = Epilogue{});
+// Fused split and product on CTA pairs (K a multiple of 8, x and W 16-byte
+// aligned); preferred for more than 128 rows once the output fills about a
+// wave of tiles.
+bool fused_pair_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
+comp_status_t launch_fused_pair(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
+                                const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi = Epilogue{});
+// variant: 0 automatic, 1 TMA loads, 2 plain loads (both one CTA per tile),
+// 3 operands swapped with the split fused (M <= 32), 4 CTA pairs with the
+// split fused.
 comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                              int variant, const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi = Epilogue{});
 

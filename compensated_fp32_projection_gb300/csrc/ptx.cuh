@@ -413,4 +413,49 @@ __device__ __forceinline__ bool mbar_try_wait_acquire_cluster(uint64_t* bar, uin
     return ok != 0;
 }
 
+// The same exchange restricted to shared memory (lighter than a release or an
+// acquire over all memory at cluster scope): a release fence that orders this
+// thread's earlier shared-memory accesses of its own CTA, then a relaxed
+// arrival on an mbarrier of any CTA of the cluster; on the other side, a
+// relaxed wait at cluster scope, then an acquire fence that orders later
+// accesses to the cluster's shared memory.
+__device__ __forceinline__ void mbar_arrive_release_smem_cluster(uint32_t cluster_addr)
+{
+    asm volatile(
+        "fence.release.sync_restrict::shared::cta.cluster;\n\t"
+        "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_relaxed_cluster(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait_relaxed_cluster(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void fence_acquire_smem_cluster()
+{
+    asm volatile("fence.acquire.sync_restrict::shared::cluster.cluster;" ::: "memory");
+}
+
 }  // namespace compfp32

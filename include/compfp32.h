@@ -111,7 +111,11 @@ comp_status_t comp_geglu_f32(const float* gate, const float* up, float* out, int
  * in tensor memory, and the merge is the epilogue.  For at most 32 rows
  * against at least 32 * 128 rows of W (K a multiple of 8, x and W 16-byte
  * aligned) the kernel swaps the operands (y^T = W x^T, 128 rows of W per MMA)
- * and splits each K block of x into shared memory as it streams W.  The accumulation order of
+ * and splits each K block of x into shared memory as it streams W.  For more
+ * than 128 rows, once the output fills about one wave of 128 x 192 tiles (same
+ * operand conditions), a cluster of two CTAs computes each 256-row tile with
+ * one instruction stream for both SMs' tensor cores; x arrives in FP32 and is
+ * split in place in shared memory.  The accumulation order of
  * the tensor cores is not specified; results agree with an FP64 evaluation of
  * the same formula to within 4e-6 * sum_k |x[m,k]| |W[n,k]| per element.
  * Errors: COMP_ERR_INVALID_VALUE if a size is negative, M*K, N*K or M*N
@@ -138,8 +142,10 @@ comp_status_t comp_gemm_f32_simt(const float* x, const uint16_t* W, float* y, in
  *       x and W and K % 8 == 0, else COMP_ERR_INVALID_VALUE),
  *   2 = plain coalesced loads (any alignment and size),
  *   3 = the swapped-operand kernel with the split fused (M <= 32, 16-byte
- *       aligned x and W, K % 8 == 0, else COMP_ERR_INVALID_VALUE).
- * A variant outside 0..3 is COMP_ERR_INVALID_VALUE.
+ *       aligned x and W, K % 8 == 0, else COMP_ERR_INVALID_VALUE),
+ *   4 = CTA pairs on 256-row tiles with the split fused (16-byte aligned x
+ *       and W, K % 8 == 0, else COMP_ERR_INVALID_VALUE).
+ * A variant outside 0..4 is COMP_ERR_INVALID_VALUE.
  */
 comp_status_t comp_gemm_f32x16_variant(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N,
                                        int64_t K, int variant, comp_stream_t stream);

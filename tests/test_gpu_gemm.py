@@ -253,3 +253,86 @@ def test_fused_swapped_rejects(pkg):
         pkg.comp_gemm_f32x16_variant(torch.zeros(4, 60, device="cuda"), torch.zeros(4096, 60, dtype=torch.float16,
                                                                                    device="cuda"), 3)
 
+
+
+# More than 128 rows: the split fused into the CTA-pair kernel (variant 4;
+# automatic once the output fills about a wave of 128 x 192 tiles).  One pair
+# tile, ragged M, N and K tails, K below one 64-wide block, one row, rows
+# that fill only the leader CTA of a pair.
+PAIRED = [(256, 448, 64), (300, 500, 200), (1, 256, 8), (130, 224, 72), (513, 1000, 1032), (1024, 2048, 520),
+          (8, 384, 256), (777, 4100, 136)]
+
+
+@pytest.mark.parametrize("shape", PAIRED, ids=lambda s: "x".join(map(str, s)))
+def test_fused_pair(pkg, orc, shape):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=M * 7 + N * 3 + K, scale=2.0)
+    y = pkg.comp_gemm_f32x16_variant(x.cuda(), W.cuda(), 4)
+    e_gpu, e_cast = check_comp(y, x, W, orc)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+
+
+@pytest.mark.parametrize("shape", [(512, 1024, 1024), (300, 500, 200), (1024, 2048, 520), (2048, 4096, 1024)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_fused_pair_equals_split_then_pair_product(pkg, shape):
+    # the in-place split is the arithmetic of comp_split_f32, and the tiles,
+    # stages, chunks and promotion are those of the two-pass pair product:
+    # bit-identical y
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=M + N + K, scale=3.0)
+    x, W = x.cuda(), W.cuda()
+    hi, lo = pkg.comp_split_f32(x)
+    y2 = pkg.comp_gemm_f16x2_variant(hi, lo, W, 2)
+    y1 = pkg.comp_gemm_f32x16_variant(x, W, 4)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+
+
+def test_fused_pair_repeatable(pkg):
+    # several calls, each reusing every stage many times: identical bits
+    # (a stage read before its split finished would show up as a difference)
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.random_case(2048, 2048, 2048, seed=21, scale=3.0)
+    x, W = x.cuda(), W.cuda()
+    y0 = pkg.comp_gemm_f32x16_variant(x, W, 4)
+    for _ in range(4):
+        y = pkg.comp_gemm_f32x16_variant(x, W, 4)
+        assert torch.equal(y.view(torch.int32), y0.view(torch.int32))
+
+
+def test_fused_pair_special_values(pkg, orc):
+    # the tiny workload's hand-set x values through the in-place split
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs("tiny")
+    y = pkg.comp_gemm_f32x16_variant(x.cuda(), W.cuda(), 4)
+    e_gpu, e_cast = check_comp(y, x, W, orc)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+
+
+def test_fused_pair_is_the_automatic_choice_for_the_square_shape(pkg):
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs("square")
+    x, W = x.cuda(), W.cuda()
+    y0 = pkg.comp_gemm_f32x16(x, W)
+    y4 = pkg.comp_gemm_f32x16_variant(x, W, 4)
+    assert torch.equal(y0.view(torch.int32), y4.view(torch.int32))
+
+
+def test_fused_pair_rejects(pkg):
+    from compensated_fp32_projection_gb300 import CompError
+
+    with pytest.raises(CompError):  # K % 8 != 0
+        pkg.comp_gemm_f32x16_variant(torch.zeros(256, 60, device="cuda"),
+                                     torch.zeros(256, 60, dtype=torch.float16, device="cuda"), 4)
+    with pytest.raises(CompError):  # x not 16-byte aligned
+        xb = torch.zeros(256 * 64 + 1, device="cuda")
+        pkg.comp_gemm_f32x16_variant(xb[1:].view(256, 64), torch.zeros(256, 64, dtype=torch.float16, device="cuda"), 4)
+    with pytest.raises(CompError):
+        pkg.comp_gemm_f32x16_variant(torch.zeros(256, 64, device="cuda"),
+                                     torch.zeros(256, 64, dtype=torch.float16, device="cuda"), 5)
