@@ -9,7 +9,20 @@
 //     additions instead of one long chain of cooperative-matrix multiply-adds,
 //     which removes the accumulation drift of long dot products.
 //
-// A persistent CTA computes 128 x BN tiles of y.  Per tile and K block of 64:
+// The kernels of this file, in order:
+//   comp_gemm_kernel         fused, one CTA per 128 x BN tile (below; also
+//                            the plain-load form for any alignment and K);
+//   comp_f16x2_kernel,       the products and merge from split planes (the
+//   comp_f16x2_splitk_kernel second pass of the two-pass form), one CTA per
+//                            tile, or K split over a cluster for <= 32 rows;
+//   comp_f16x2_pair_kernel   the same on CTA pairs (256-row tiles);
+//   comp_f32x16_pair_kernel  fused on CTA pairs: FP32 x split in place in
+//                            the pair product's stages;
+//   comp_f16x2_swap_kernel   operands swapped for <= 32 rows, optionally with
+//                            the split fused.
+//
+// comp_gemm_kernel: a persistent CTA computes 128 x BN tiles of y.  Per tile
+// and K block of 64:
 //   1. TMA brings the 128 x 64 FP32 block of x (two 128x32 boxes, 128-byte
 //      swizzle) into a 4-deep shared-memory ring, and the BN x 64 FP16 box of W
 //      into another 4-deep ring;
