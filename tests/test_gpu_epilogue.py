@@ -93,6 +93,23 @@ def test_projection_paths_apply_the_epilogue(pkg, orc, shape, ws):
     check_epilogue(out, x, W, b, gate, orc)
 
 
+def test_fused_pair_epilogue_equals_two_pass(pkg, orc):
+    # without a workspace a large projection runs the fused CTA-pair kernel
+    # (bias in its epilogue, then the GEGLU dispatch); with one, the two-pass
+    # form on CTA pairs: same tiles, chunks and epilogue, so identical bits
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = 300, 12800, 136
+    x, W = workloads.random_case(M, N, K, seed=31, scale=2.0)
+    b, gate = operands(M, N, True, True, seed=7)
+    x, W, b, gate = x.cuda(), W.cuda(), b.cuda(), gate.cuda()
+    none = torch.empty(16, dtype=torch.uint8, device="cuda")
+    y_fused = pkg.comp_gemm_f32x16_epilogue(x, W, b, gate, workspace=none)
+    y_two = pkg.comp_gemm_f32x16_epilogue(x, W, b, gate)
+    assert torch.equal(y_fused.view(torch.int32), y_two.view(torch.int32))
+    check_epilogue(y_fused, x.cpu(), W.cpu(), b.cpu(), gate.cpu(), orc)
+
+
 def test_no_operands_is_the_plain_projection(pkg):
     from compensated_fp32_projection_gb300 import workloads
 
