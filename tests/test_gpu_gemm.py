@@ -190,6 +190,22 @@ def test_simt_true_fp32(pkg, orc, shape):
     assert np.all(np.abs(y - y_true) <= gamma * den + 2.0**-149)
 
 
+def test_simt_vector_and_scalar_loads_agree_bitwise(pkg):
+    # 16-byte loads (x and W aligned, K % 8 == 0) and bounds-checked scalar
+    # loads (x moved off 16-byte alignment) stage the same values, and the
+    # multiply-adds run in the same order: identical bits
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.random_case(300, 520, 264, seed=19, scale=2.0)
+    xa, Wd = x.cuda(), W.cuda()
+    buf = torch.empty(x.numel() + 1, device="cuda")
+    xm = buf[1:].view(x.shape)
+    xm.copy_(xa)
+    y1 = pkg.comp_gemm_f32_simt(xa, Wd)
+    y2 = pkg.comp_gemm_f32_simt(xm, Wd)
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+
+
 def test_device_status_clean_after_gemms(pkg):
     st, where = pkg.device_status()
     assert st == 0 and where == 0
