@@ -458,6 +458,21 @@ def run_ours(args):
     o32 = torch.empty(n, device=dev)
     med, mean = time_kernel(lambda: pkg.comp_merge_f32(a32, b32, o32), flush, stream, 20)
     merge_gbs = 12.0 * n / (mean * 1e-3) / 1e9
+    del xs, hi, lo, a32, b32, o32
+    # the labelled sweep point far beyond L2: n = 2^28 (1 GiB of x; 3 GiB read
+    # and written by the merge)
+    nb = 1 << 28
+    xs = torch.randn(nb, device=dev)
+    hi = torch.empty(nb, dtype=torch.float16, device=dev)
+    lo = torch.empty(nb, dtype=torch.float16, device=dev)
+    med, mean = time_kernel(lambda: pkg.comp_split_f32(xs, hi, lo), flush, stream, 10)
+    split_big_gbs = 8.0 * nb / (mean * 1e-3) / 1e9
+    del hi, lo
+    a32 = xs
+    b32 = torch.randn(nb, device=dev)
+    o32 = torch.empty(nb, device=dev)
+    med, mean = time_kernel(lambda: pkg.comp_merge_f32(a32, b32, o32), flush, stream, 10)
+    merge_big_gbs = 12.0 * nb / (mean * 1e-3) / 1e9
     med, fused_ms = time_kernel(lambda: pkg.comp_gemm_f32x16(x, W, y), flush, stream, 50)
     fused_tflops = flops / (fused_ms * 1e-3) / 1e12
     med, mean = time_kernel(lambda: pkg.comp_gemm_f32_simt(x, W, y), flush, stream, 3, warm=1)
@@ -475,7 +490,7 @@ def run_ours(args):
     med, mean_geglu = time_kernel(lambda: pkg.comp_geglu_f32(gate_ep, up_ep, out_ep), flush, stream, 20)
     geglu_gbs = 12.0 * s.M * s.N / (mean_geglu * 1e-3) / 1e9
     del b_ep, gate_ep, up_ep, out_ep
-    del xs, hi, lo, a32, b32, o32
+    del xs, a32, b32, o32
 
     # the other configurations (parity cases), each through the workspace entry
     # point with the same flush; roofline time t* = max(tensor work / tensor peak,
@@ -581,6 +596,10 @@ def run_ours(args):
                 "frac_of_roofline": fused_tflops / (peaks["bf16_tflops"] / 2.0)},
             "comp_split_f32": {"n": n, "GB/s": split_gbs, "frac_of_hbm": split_gbs / peaks["hbm_gbs"]},
             "comp_merge_f32": {"n": n, "GB/s": merge_gbs, "frac_of_hbm": merge_gbs / peaks["hbm_gbs"]},
+            "comp_split_f32 (n = 2^28, beyond L2)": {"n": nb, "GB/s": split_big_gbs,
+                                                     "frac_of_hbm": split_big_gbs / peaks["hbm_gbs"]},
+            "comp_merge_f32 (n = 2^28, beyond L2)": {"n": nb, "GB/s": merge_big_gbs,
+                                                     "frac_of_hbm": merge_big_gbs / peaks["hbm_gbs"]},
             "comp_gemm_f32_simt": {"TFLOP/s": simt_tflops},
             "comp_geglu_f32": {"n": s.M * s.N, "GB/s": geglu_gbs, "frac_of_hbm": geglu_gbs / peaks["hbm_gbs"]},
             "comp_gemm_f32x16_epilogue (bias in the product's epilogue, then the GEGLU dispatch)": {
