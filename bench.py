@@ -398,20 +398,23 @@ def run_ours(args):
     # end to end through the public API, pipelined like a serving loop: step i's
     # inputs go up on one copy stream while step i-1 computes and step i-2's
     # result comes down on another.  Every step still copies its own x and W
-    # from pinned host memory and its own y back; two buffer sets, each reused
-    # only after its previous result has left the device.
+    # from pinned host memory and its own y back; three buffer sets, each reused
+    # only after its previous result has left the device (with two, the upload
+    # of step i+1 waits for the download of step i-1 and the link idles).
+    nbuf = 3
     x_h = x_cpu.pin_memory()
     W_h = W_cpu.pin_memory()
-    y_h = [torch.empty((s.M, s.N), dtype=torch.float32).pin_memory() for _ in range(2)]
-    bufs = [(torch.empty_like(x), torch.empty_like(W), torch.empty_like(y), torch.empty_like(ws)) for _ in range(2)]
+    y_h = [torch.empty((s.M, s.N), dtype=torch.float32).pin_memory() for _ in range(nbuf)]
+    bufs = [(torch.empty_like(x), torch.empty_like(W), torch.empty_like(y), torch.empty_like(ws))
+            for _ in range(nbuf)]
     s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
 
     def run_e2e(nsteps):
-        done_out = [None, None]
+        done_out = [None] * nbuf
         for i in range(nsteps):
-            xb, Wb, yb, wsb = bufs[i % 2]
-            if done_out[i % 2] is not None:
-                s_in.wait_event(done_out[i % 2])
+            xb, Wb, yb, wsb = bufs[i % nbuf]
+            if done_out[i % nbuf] is not None:
+                s_in.wait_event(done_out[i % nbuf])
             with torch.cuda.stream(s_in):
                 xb.copy_(x_h, non_blocking=True)
                 Wb.copy_(W_h, non_blocking=True)
@@ -423,14 +426,14 @@ def run_ours(args):
             ev_c.record(s_comp)
             s_out.wait_event(ev_c)
             with torch.cuda.stream(s_out):
-                y_h[i % 2].copy_(yb, non_blocking=True)
+                y_h[i % nbuf].copy_(yb, non_blocking=True)
             ev_o = torch.cuda.Event()
             ev_o.record(s_out)
-            done_out[i % 2] = ev_o
+            done_out[i % nbuf] = ev_o
         return done_out
 
-    e2e_steps = max(3, min(args.steps, 30))
-    run_e2e(2)
+    e2e_steps = max(3, min(args.steps, 60))
+    run_e2e(nbuf)
     barrier()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
@@ -584,7 +587,7 @@ def run_ours(args):
             "h2d_bytes_per_step": 4 * s.M * s.K + 2 * s.N * s.K,
             "d2h_bytes_per_step": 4 * s.M * s.N,
             "pipeline": "comp_gemm_f32x16_ws on a compute stream; inputs up and results down on two copy streams, "
-                        "two buffer sets",
+                        "three buffer sets",
         },
         "gpu_launches": 2 * args.steps,
         "kernels": {
