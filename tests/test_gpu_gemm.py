@@ -307,6 +307,17 @@ def test_fused_pair_equals_split_then_pair_product(pkg, shape):
     assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
 
 
+def test_fused_pair_encoder_outliers(pkg, orc):
+    # the encoder workload (1 % of x scaled by 100) through the in-place split
+    # on CTA pairs, every output against the oracle
+    from compensated_fp32_projection_gb300 import workloads
+
+    x, W = workloads.make_inputs("encoder")
+    y = pkg.comp_gemm_f32x16_variant(x.cuda(), W.cuda(), 4)
+    e_gpu, e_cast = check_comp(y, x, W, orc)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+
+
 def test_fused_pair_repeatable(pkg):
     # several calls, each reusing every stage many times: identical bits
     # (a stage read before its split finished would show up as a difference)
