@@ -4,8 +4,10 @@
 // the CUDA cores, summed in increasing k.  W is widened to FP32 exactly.
 //
 // Shared-memory tiled: a 128x128 output tile per 256-thread block, 8x8
-// outputs per thread, K step 16, operands staged k-major in shared memory
-// (rows padded to 132 floats) and double-buffered through registers.  A warp
+// outputs per thread (multiply-adds issued two at a time as packed
+// fma.rn.f32x2, each lane an ordinary binary32 fused multiply-add), K step
+// 16, operands staged k-major in shared memory (rows padded to 132 floats)
+// and double-buffered through registers.  A warp
 // covers 4 x 8 threads of the 16 x 16 thread grid, so that its operand loads
 // from shared memory are one wavefront each.
 // Global loads: with K % 8 == 0 and 16-byte aligned x and W, coalesced
@@ -22,6 +24,22 @@ namespace {
 
 constexpr int TBM = 128, TBN = 128, TBK = 16, kThreads = 256;
 constexpr int kLd = TBM + 4;  // padded row of a k-major operand tile (floats)
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+
+// c0 = fma(a, b0, c0), c1 = fma(a, b1, c1): two independent binary32 fused
+// multiply-adds, each rounded to nearest even, in one packed instruction
+// (the same results as two scalar fmaf; half the issue slots).
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a, float b0, float b1)
+{
+    uint64_t c;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(c) : "l"(f2_pack(a, a)), "l"(f2_pack(b0, b1)), "l"(f2_pack(c0, c1)));
+    c0 = __uint_as_float(static_cast<uint32_t>(c));
+    c1 = __uint_as_float(static_cast<uint32_t>(c >> 32));
+}
 
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads, 2) gemm_simt_kernel(const float* __restrict__ x,
@@ -129,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_simt_kernel(const float* __r
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < 8; j += 2)
+                    fma2(acc[i][j], acc[i][j + 1], a[i], b[j], b[j + 1]);
         }
         if (kt + 1 < nk)
             stage(buf ^ 1);
