@@ -16,7 +16,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kBlocksPerSm = 8;
-constexpr int kUnroll = 2;
+constexpr int kUnroll = 4;
 
 __device__ __forceinline__ float geglu1(float g, float u)
 {
