@@ -274,9 +274,10 @@ def test_fused_swapped_rejects(pkg):
 # More than 128 rows: the split fused into the CTA-pair kernel (variant 4;
 # automatic once the output fills about a wave of 128 x 192 tiles).  One pair
 # tile, ragged M, N and K tails, K below one 64-wide block, one row, rows
-# that fill only the leader CTA of a pair.
+# that fill only the leader CTA of a pair, and a long K (128 chunks of
+# promotion) that still has to beat the FP16 cast by 100x.
 PAIRED = [(256, 448, 64), (300, 500, 200), (1, 256, 8), (130, 224, 72), (513, 1000, 1032), (1024, 2048, 520),
-          (8, 384, 256), (777, 4100, 136)]
+          (8, 384, 256), (777, 4100, 136), (256, 448, 16384)]
 
 
 @pytest.mark.parametrize("shape", PAIRED, ids=lambda s: "x".join(map(str, s)))
