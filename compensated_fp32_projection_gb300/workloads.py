@@ -150,5 +150,29 @@ def random_bits_f32(n: int, seed: int) -> torch.Tensor:
     return b.view(torch.float32)
 
 
+def special_values_f32(n: int, seed: int) -> torch.Tensor:
+    """n finite FP32 values below 65504 in magnitude that stress an FP16 split:
+    a quarter are the midpoints between neighbouring FP16 values (ties) or the
+    FP32 values just beside them; 1000 lie in [65000, 65504]; 1000 are drawn
+    from N(0, 1e-6) (FP16-subnormal hi and lo); the rest are random bit
+    patterns with binary exponents -30 .. 14 (2^-30 <= |x| < 32768, so FP16
+    subnormals as well as normals).  Signs random."""
+    g = torch.Generator().manual_seed(seed)
+    ri = lambda hi, size: torch.randint(0, hi, size, generator=g, dtype=torch.int64)  # noqa: E731
+    bits = (ri(2, (n,)) << 31) | ((97 + ri(45, (n,))) << 23) | ri(1 << 23, (n,))
+    x = bits.to(torch.int64).to(torch.int32).view(torch.float32).clone()
+    k = n // 4
+    h = ri(0x7bff, (k,)).to(torch.int16).view(torch.float16)  # finite, positive, below 65504
+    up = (h.view(torch.int16) + 1).view(torch.float16)        # the next FP16 value up
+    mid = ((h.double() + up.double()) / 2).float()            # an exact tie in FP32
+    side = ri(3, (k,))
+    mid = torch.where(side == 1, torch.nextafter(mid, torch.full_like(mid, float("inf"))), mid)
+    mid = torch.where(side == 2, torch.nextafter(mid, torch.zeros_like(mid)), mid)
+    x[:k] = mid * torch.where(ri(2, (k,)) == 0, 1.0, -1.0)
+    x[k:k + 1000] = torch.linspace(65000.0, 65504.0, 1000)
+    x[k + 1000:k + 2000] = torch.randn(1000, generator=g) * 1e-6
+    return x
+
+
 def sha256(t: torch.Tensor) -> str:
     return hashlib.sha256(t.contiguous().view(torch.uint8).numpy().tobytes()).hexdigest()

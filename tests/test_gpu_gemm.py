@@ -364,3 +364,20 @@ def test_fused_pair_rejects(pkg):
     with pytest.raises(CompError):
         pkg.comp_gemm_f32x16_variant(torch.zeros(256, 64, device="cuda"),
                                      torch.zeros(256, 64, dtype=torch.float16, device="cuda"), 5)
+
+
+@pytest.mark.parametrize("variant,M", [(1, 512), (2, 512), (3, 32), (4, 512)], ids=["tma", "plain", "swapped", "pairs"])
+def test_fused_split_bit_exact_through_identity(pkg, orc, variant, M):
+    # With W = I each output is hi + 2^-10 lo of one x value, a sum that is
+    # exact in FP32 (about 22 significant bits), so every fused kernel's
+    # in-kernel split must give the oracle's bits for each of M*K values that
+    # stress it: FP16 ties and their neighbours, FP16-subnormal hi and lo,
+    # magnitudes up to 65504
+    from compensated_fp32_projection_gb300 import workloads
+
+    K = 2048
+    x = workloads.special_values_f32(M * K, seed=variant).reshape(M, K)
+    W = torch.eye(K, dtype=torch.float16)
+    y = pkg.comp_gemm_f32x16_variant(x.cuda(), W.cuda(), variant).cpu().numpy()
+    y_or = orc.gemm_comp(x.numpy(), W.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(y.view(np.uint32), y_or.view(np.uint32)), int(np.sum(y.view(np.uint32) != y_or.view(np.uint32)))

@@ -325,3 +325,19 @@ def test_split_k_deterministic(pkg, shape):
     y1 = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), 1)
     y2 = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), 1)
     assert torch.equal(bits(y1), bits(y2))
+
+
+@pytest.mark.parametrize("variant,M", [(1, 512), (2, 512), (3, 32)], ids=["one-cta", "pairs", "swapped"])
+def test_product_bit_exact_through_identity(pkg, orc, variant, M):
+    # W = I: each output is hi + 2^-10 lo of one x value, exact in FP32, so
+    # split + product must give the oracle's bits on values that stress the
+    # split (FP16 ties, FP16-subnormal hi and lo, magnitudes up to 65504)
+    from compensated_fp32_projection_gb300 import workloads
+
+    K = 2048
+    x = workloads.special_values_f32(M * K, seed=10 + variant).reshape(M, K)
+    W = torch.eye(K, dtype=torch.float16)
+    hi, lo = pkg.comp_split_f32(x.cuda())
+    y = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), variant).cpu().numpy()
+    y_or = orc.gemm_comp(x.numpy(), W.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(y.view(np.uint32), y_or.view(np.uint32)), int(np.sum(y.view(np.uint32) != y_or.view(np.uint32)))
