@@ -185,6 +185,41 @@ def test_split_then_merge_reconstructs(pkg):
     assert torch.all((y.double() - xd).abs() <= 2.0**-22 * xd.abs() + 2.0**-35)
 
 
+# Beyond 2^31 elements (64-bit indexing in the grid-stride loops), odd so that
+# the scalar tail runs too; inputs drawn on the device, ~1 M sampled indices
+# (the first, the last and random ones) checked against the oracle.
+N_BIG = (1 << 31) + 8191
+
+
+def _big_sample(n):
+    rng = np.random.default_rng(31)
+    idx = np.concatenate([np.arange(4096), np.arange(n - 16384, n), rng.integers(0, n, 1 << 20)])
+    return torch.from_numpy(np.unique(idx).astype(np.int64))
+
+
+def test_split_beyond_2_31_elements(pkg, orc):
+    g = torch.Generator(device="cuda").manual_seed(5)
+    x = torch.randn(N_BIG, device="cuda", generator=g) * 100
+    hi, lo = pkg.comp_split_f32(x)
+    idx = _big_sample(N_BIG).cuda()
+    x_np = x[idx].cpu().numpy()
+    assert_split_equal(x_np, hi[idx].cpu(), lo[idx].cpu(), orc)
+    del x, hi, lo
+    torch.cuda.empty_cache()
+
+
+def test_merge_beyond_2_31_elements(pkg, orc):
+    g = torch.Generator(device="cuda").manual_seed(6)
+    a = torch.randn(N_BIG, device="cuda", generator=g)
+    b = torch.randn(N_BIG, device="cuda", generator=g) * 1e3
+    y = pkg.comp_merge_f32(a, b)
+    idx = _big_sample(N_BIG).cuda()
+    ref = orc.merge(a[idx].cpu().numpy(), b[idx].cpu().numpy())
+    assert np.array_equal(y[idx].cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    del a, b, y
+    torch.cuda.empty_cache()
+
+
 def test_device_status_clean(pkg):
     st, where = pkg.device_status()
     assert st == 0 and where == 0
