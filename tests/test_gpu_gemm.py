@@ -381,3 +381,26 @@ def test_fused_split_bit_exact_through_identity(pkg, orc, variant, M):
     y = pkg.comp_gemm_f32x16_variant(x.cuda(), W.cuda(), variant).cpu().numpy()
     y_or = orc.gemm_comp(x.numpy(), W.view(torch.int16).numpy().view(np.uint16))
     assert np.array_equal(y.view(np.uint32), y_or.view(np.uint32)), int(np.sum(y.view(np.uint32) != y_or.view(np.uint32)))
+
+
+def test_projection_beyond_2_31_activation_elements(pkg, orc):
+    # M*K > 2^31 (64-bit offsets in every path): the fused CTA-pair kernel (the
+    # automatic choice) and the two-pass form with a workspace, ~3,000 sampled
+    # outputs (first and last rows included) against the oracle
+    M, N, K = 524289, 264, 4096
+    g = torch.Generator(device="cuda").manual_seed(9)
+    x = torch.randn(M, K, device="cuda", generator=g)
+    W = (torch.randn(N, K, device="cuda", generator=g) * 0.02).half()
+    r, c = sample_outputs(M, N)
+    rows = np.unique(r)
+    x_rows = x[torch.from_numpy(rows).cuda()].cpu()  # only the sampled rows go to the oracle
+    r_local = np.searchsorted(rows, r)
+    for y in (pkg.comp_gemm_f32x16(x, W), pkg.comp_gemm_f32x16_ws(x, W)):
+        ys = y[torch.from_numpy(r).cuda(), torch.from_numpy(c).cuda()].cpu()
+        yfull = torch.zeros(rows.size, N)
+        yfull[torch.from_numpy(r_local), torch.from_numpy(c)] = ys
+        e_gpu, e_cast = check_comp(yfull, x_rows, W.cpu(), orc, r_local, c)
+        assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+        del y
+    del x
+    torch.cuda.empty_cache()
