@@ -404,3 +404,25 @@ def test_projection_beyond_2_31_activation_elements(pkg, orc):
         del y
     del x
     torch.cuda.empty_cache()
+
+
+def test_projection_beyond_2_31_weight_elements(pkg, orc):
+    # N*K > 2^31 with 16 rows: the swapped-operand kernel with the split fused
+    # (the automatic choice), ~3,000 sampled outputs (last columns included)
+    # against the oracle
+    M, N, K = 16, 524289, 4096
+    g = torch.Generator(device="cuda").manual_seed(10)
+    x = torch.randn(M, K, device="cuda", generator=g)
+    W = (torch.randn(N, K, device="cuda", generator=g) * 0.02).half()
+    y = pkg.comp_gemm_f32x16(x, W)
+    r, c = sample_outputs(M, N)
+    cols = np.unique(c)
+    W_cols = W[torch.from_numpy(cols).cuda()].cpu()  # only the sampled rows of W go to the oracle
+    c_local = np.searchsorted(cols, c)
+    ys = y[torch.from_numpy(r).cuda(), torch.from_numpy(c).cuda()].cpu()
+    ysub = torch.zeros(M, cols.size)
+    ysub[torch.from_numpy(r), torch.from_numpy(c_local)] = ys
+    e_gpu, e_cast = check_comp(ysub, x.cpu(), W_cols, orc, r, c_local)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+    del W, y
+    torch.cuda.empty_cache()
