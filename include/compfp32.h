@@ -220,11 +220,11 @@ comp_status_t comp_gemm_f32x16_ws(const float* x, const uint16_t* W, float* y, i
                                   void* workspace, int64_t workspace_bytes, comp_stream_t stream);
 
 /*
- * comp_gemm_f32x16_epilogue — the projection of comp_gemm_f32x16_ws followed,
- * inside the product kernel's epilogue, by the FP32 operations of a GEGLU
- * feed-forward step (laya.cpp docs/vulkan.md, feed-forward paragraph: the gate
- * activation and multiplication are fused into one dispatch, with no separate
- * copies or passes):
+ * comp_gemm_f32x16_epilogue — the projection of comp_gemm_f32x16_ws followed
+ * by the FP32 operations of a GEGLU feed-forward step (laya.cpp
+ * docs/vulkan.md, feed-forward paragraph: the gate activation and
+ * multiplication are fused into one dispatch, with no separate copies or
+ * passes):
  *   out[m,n] = gelu(gate[m,n]) * (y[m,n] + bias[n]),
  *   gelu(g) = g * Phi(g), Phi(g) = erfc(-g / sqrt 2) / 2 (the exact GELU),
  * with y the compensated projection.  Each operation is an FP32 operation
