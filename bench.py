@@ -49,6 +49,9 @@ KERNEL_SOURCE = os.path.join(ROOT, "compensated_fp32_projection_gb300", "csrc", 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+LEGS = ("step", "split", "product", "fused", "ws", "merge", "simt", "geglu")
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -56,7 +59,74 @@ def parse():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
+    p.add_argument("--leg", choices=LEGS, default=None,
+                   help="time one leg alone on one shape (a small process for profiler captures); prints one "
+                        "diagnostic line, not the bench line")
+    p.add_argument("--config", default=WORKLOAD, help="shape of --leg: tiny, encoder, square, skinny, nonaligned")
     return p.parse_args()
+
+
+def source_sha256():
+    """SHA-256 over the library's sources, the header and this file (the GPU machine's
+    copy of the repository has no git metadata)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "compensated_fp32_projection_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)) + [
+        os.path.join(ROOT, "include", "compfp32.h"), os.path.abspath(__file__)]
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def run_metadata(dev):
+    """GPU, driver, CUDA, SM count, source revision and host CPU of this run."""
+    import platform
+
+    import torch
+
+    props = torch.cuda.get_device_properties(dev)
+    meta = {"gpu": props.name, "sm_count": props.multi_processor_count,
+            "compute_capability": f"{props.major}.{props.minor}",
+            "torch": torch.__version__, "cuda_runtime_torch": torch.version.cuda,
+            "source_sha256": source_sha256(), "host_arch": platform.machine()}
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(dev.index), "--query-gpu=driver_version",
+                              "--format=csv,noheader"], capture_output=True, text=True, timeout=20)
+        meta["driver"] = out.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        meta["driver"] = None
+    try:
+        out = subprocess.run(["nvcc", "--version"], capture_output=True, text=True, timeout=20)
+        meta["nvcc"] = out.stdout.strip().splitlines()[-1] if out.stdout.strip() else None
+    except (OSError, subprocess.SubprocessError):
+        meta["nvcc"] = None
+    try:
+        out = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True, text=True, timeout=20)
+        meta["git_sha"] = out.stdout.strip() if out.returncode == 0 else None
+    except (OSError, subprocess.SubprocessError):
+        meta["git_sha"] = None
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20)
+        for line in out.stdout.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    meta["host_cpu"] = model
+    meta["host_cores"] = os.cpu_count()
+    return meta
 
 
 def dist_env():
@@ -535,6 +605,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
+    meta = run_metadata(dev)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = oracle_cpu_baseline(x_cpu, W_cpu)
@@ -616,16 +687,75 @@ def run_ours(args):
         line["clocks"] = clocks
     if cpu is not None:
         line["cpu_baseline"] = cpu
+        line["cpu_baseline"]["host_cpu"] = meta.get("host_cpu")
+    line["run"] = meta
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
 
 
+def run_leg(args):
+    """One leg on one shape, W warm-up and K timed launches (each with its own
+    CUDA-event pair, L2 flushed before each, outside the pair); prints one
+    diagnostic line.  Sized for profiler captures: only this leg's buffers are
+    allocated."""
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import compensated_fp32_projection_gb300 as pkg
+    from compensated_fp32_projection_gb300 import workloads
+
+    s = workloads.SHAPES[args.config]
+    x_cpu, W_cpu = workloads.make_inputs(args.config)
+    x, W = x_cpu.to(dev), W_cpu.to(dev)
+    y = torch.empty((s.M, s.N), dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    leg = args.leg
+    if leg in ("step", "split", "product"):
+        ws = torch.empty(pkg.comp_gemm_workspace_bytes(s.M, s.K), dtype=torch.uint8, device=dev)
+        hi = ws[: 2 * s.M * s.K].view(torch.float16).view(s.M, s.K)
+        lo = ws[2 * s.M * s.K:].view(torch.float16).view(s.M, s.K)
+        pkg.comp_split_f32(x, hi, lo)
+        fns = {"step": lambda: (pkg.comp_split_f32(x, hi, lo), pkg.comp_gemm_f16x2(hi, lo, W, y)),
+               "split": lambda: pkg.comp_split_f32(x, hi, lo),
+               "product": lambda: pkg.comp_gemm_f16x2(hi, lo, W, y)}
+        fn = fns[leg]
+        work = 2.0 * s.M * s.N * s.K if leg != "split" else 8.0 * s.M * s.K
+    elif leg == "fused":
+        fn, work = (lambda: pkg.comp_gemm_f32x16(x, W, y)), 2.0 * s.M * s.N * s.K
+    elif leg == "ws":
+        wso = torch.empty(max(16, pkg.comp_gemm_workspace_bytes_mnk(s.M, s.N, s.K)), dtype=torch.uint8, device=dev)
+        fn, work = (lambda: pkg.comp_gemm_f32x16_ws(x, W, y, workspace=wso)), 2.0 * s.M * s.N * s.K
+    elif leg == "simt":
+        fn, work = (lambda: pkg.comp_gemm_f32_simt(x, W, y)), 2.0 * s.M * s.N * s.K
+    elif leg in ("merge", "geglu"):
+        a = torch.randn(s.M * s.N, device=dev)
+        b = torch.randn(s.M * s.N, device=dev)
+        o = torch.empty_like(a)
+        fn = (lambda: pkg.comp_merge_f32(a, b, o)) if leg == "merge" else (lambda: pkg.comp_geglu_f32(a, b, o))
+        work = 12.0 * s.M * s.N
+    med, mean = time_kernel(fn, flush, stream, max(1, args.steps), warm=max(1, args.warmup))
+    st, where = pkg.device_status()
+    if st != 0:
+        raise RuntimeError(f"kernel fault word {where:#x}")
+    unit = "GB/s" if leg in ("split", "merge", "geglu") else "eff TFLOP/s"
+    rate = work / (med * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
+    print(json.dumps({"leg": leg, "config": args.config, "M": s.M, "N": s.N, "K": s.K, "launches": args.steps,
+                      "us_median": med * 1e3, "us_mean": mean * 1e3, unit: rate}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.leg is not None:
+        run_leg(args)
     else:
         run_ours(args)
 

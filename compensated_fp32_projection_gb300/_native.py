@@ -14,10 +14,11 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcompfp32
 
 COMP_OK = 0
 COMP_ERR_INVALID_VALUE = 1
-COMP_ERR_UNSUPPORTED_DEVICE = 2
-COMP_ERR_LAUNCH = 3
-COMP_ERR_TIMEOUT = 4
-COMP_ERR_CUDA = 5
+COMP_ERR_MISALIGNED = 2  # reserved, never returned
+COMP_ERR_UNSUPPORTED_DEVICE = 3
+COMP_ERR_LAUNCH = 4
+COMP_ERR_TIMEOUT = 5
+COMP_ERR_CUDA = 6
 
 # Every symbol the header declares, with its ctypes signature.
 _i64, _int, _u32, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_void_p

@@ -371,6 +371,8 @@ const char* comp_status_string(comp_status_t status)
         return "COMP_OK";
     case COMP_ERR_INVALID_VALUE:
         return "COMP_ERR_INVALID_VALUE: bad pointer, size or aliasing";
+    case COMP_ERR_MISALIGNED:
+        return "COMP_ERR_MISALIGNED: reserved (no call returns it)";
     case COMP_ERR_UNSUPPORTED_DEVICE:
         return "COMP_ERR_UNSUPPORTED_DEVICE: the current device is not an sm_103 GPU";
     case COMP_ERR_LAUNCH:

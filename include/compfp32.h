@@ -23,7 +23,9 @@
  *     CUDA half-precision header.
  *   - Every pointer is DEVICE memory owned by the caller (for example a PyTorch
  *     tensor's data pointer) on the current CUDA device.  The library keeps no
- *     pointer after a call returns, and allocates no device memory.
+ *     pointer after a call returns and allocates no device memory; the one
+ *     device reservation it has is the static 64 MiB workspace of
+ *     comp_gemm_f32x16_noalloc (see there).
  *   - Matrices are dense and row-major: x is [M, K] (K contiguous), W is [N, K]
  *     (K contiguous), y is [M, N] (N contiguous).  Any element-aligned address
  *     and any size are accepted; addresses or sizes that the fast paths cannot
@@ -50,13 +52,20 @@
 extern "C" {
 #endif
 
+/*
+ * Status codes.  The numeric values are part of the ABI and never change.
+ * COMP_ERR_MISALIGNED is reserved: every call accepts any element-aligned
+ * address and any size (a misaligned or ragged case takes a slower path and
+ * still returns COMP_OK), so no call returns it today.
+ */
 typedef enum comp_status {
     COMP_OK = 0,
     COMP_ERR_INVALID_VALUE = 1,      /* bad pointer, size or aliasing; nothing was enqueued */
-    COMP_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not sm_103 (GB300), or no device */
-    COMP_ERR_LAUNCH = 3,             /* the kernel launch itself failed */
-    COMP_ERR_TIMEOUT = 4,            /* a kernel gave up a bounded wait (see comp_device_status) */
-    COMP_ERR_CUDA = 5                /* another CUDA runtime call failed */
+    COMP_ERR_MISALIGNED = 2,         /* reserved; never returned */
+    COMP_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 (GB300), or no device */
+    COMP_ERR_LAUNCH = 4,             /* the kernel launch itself failed */
+    COMP_ERR_TIMEOUT = 5,            /* a kernel gave up a bounded wait (see comp_device_status) */
+    COMP_ERR_CUDA = 6                /* another CUDA runtime call failed */
 } comp_status_t;
 
 /* An opaque cudaStream_t. */
@@ -274,10 +283,21 @@ comp_status_t comp_gemm_f16x2_epilogue(const uint16_t* hi, const uint16_t* lo, c
  *   Same arguments, layout, results and errors as comp_gemm_f32x16, plus
  *   COMP_ERR_INVALID_VALUE when 4 * M * K exceeds
  *   COMP_NOALLOC_MAX_WORKSPACE_BYTES (rejected, never truncated).
- *   The first call on a device looks up the static array's device address
- *   (cudaGetSymbolAddress, with that device current; COMP_ERR_CUDA if it
- *   fails); make that first call before any stream capture.
- *   The array is shared by all calls on the device: calls whose executions
+ *   Paths: as comp_gemm_f32x16_ws given that workspace.  With K % 8 != 0 (or
+ *   W not 16-byte aligned) the two-pass form needs 4 * M * Kp + 2 * N * Kp
+ *   bytes, Kp = K rounded up to a multiple of 8; when that exceeds the array
+ *   the call runs the fused kernel, which needs no workspace (same results
+ *   within the same tolerance).
+ *   The array's device address belongs to a CUDA context.  The first call in
+ *   each context on a device looks it up (cudaGetSymbolAddress, with that
+ *   device current; COMP_ERR_CUDA if it fails) and caches it with the
+ *   context's identifier; make that first call before any stream capture.
+ *   After cudaDeviceReset, or from another context, the next call looks it
+ *   up again.  The array is committed when the runtime loads this library's
+ *   module that holds it into a context: at the first such call (lazy module
+ *   loading, the default), or when the context is created under
+ *   CUDA_MODULE_LOADING=EAGER.
+ *   The array is shared by all calls in a context: calls whose executions
  *   overlap (unordered streams or threads) race on it.  Calls ordered on one
  *   stream are safe.  Nothing in it needs to start at zero.
  */

@@ -40,11 +40,94 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in _native.SIGNATURES, f"binding lacks {name}"
 
 
+STATUS_VALUES = {
+    # the numbering of the boundary's status enum; part of the ABI
+    "COMP_OK": 0,
+    "COMP_ERR_INVALID_VALUE": 1,
+    "COMP_ERR_MISALIGNED": 2,
+    "COMP_ERR_UNSUPPORTED_DEVICE": 3,
+    "COMP_ERR_LAUNCH": 4,
+    "COMP_ERR_TIMEOUT": 5,
+    "COMP_ERR_CUDA": 6,
+}
+
+
+def test_status_values_pinned():
+    """Every code's numeric value in the header, and the binding's copy of it."""
+    from compensated_fp32_projection_gb300 import _native
+
+    text = open(HEADER).read()
+    body = re.search(r"typedef enum comp_status \{(.*?)\} comp_status_t;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    found = {k: int(v) for k, v in re.findall(r"(COMP_[A-Z_]+)\s*=\s*(\d+)", body)}
+    assert found == STATUS_VALUES
+    for name, value in STATUS_VALUES.items():
+        assert getattr(_native, name) == value, name
+
+
 def test_status_strings_and_version(lib):
-    for code in range(6):
+    for name, code in STATUS_VALUES.items():
         s = lib.comp_status_string(code).decode()
-        assert s.startswith("COMP_")
+        assert s.split(":")[0] == name
+    assert lib.comp_status_string(99).decode() == "unknown comp_status_t"
     assert lib.comp_version() >= 100
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "compfp32.h"
+
+static int check(comp_status_t s, int value, const char* name)
+{
+    const char* str = comp_status_string(s);
+    if ((int)s != value || strncmp(str, name, strlen(name)) != 0) {
+        printf("bad %s\n", name);
+        return 1;
+    }
+    return 0;
+}
+
+int main(void)
+{
+    int bad = 0;
+    bad += check(COMP_OK, 0, "COMP_OK");
+    bad += check(COMP_ERR_INVALID_VALUE, 1, "COMP_ERR_INVALID_VALUE");
+    bad += check(COMP_ERR_MISALIGNED, 2, "COMP_ERR_MISALIGNED");
+    bad += check(COMP_ERR_UNSUPPORTED_DEVICE, 3, "COMP_ERR_UNSUPPORTED_DEVICE");
+    bad += check(COMP_ERR_LAUNCH, 4, "COMP_ERR_LAUNCH");
+    bad += check(COMP_ERR_TIMEOUT, 5, "COMP_ERR_TIMEOUT");
+    bad += check(COMP_ERR_CUDA, 6, "COMP_ERR_CUDA");
+    /* argument errors need no device: a negative size is rejected first */
+    if (comp_split_f32((const float*)0, (uint16_t*)0, (uint16_t*)0, -1, (comp_stream_t)0) != COMP_ERR_INVALID_VALUE)
+        ++bad;
+    if (comp_gemm_workspace_bytes(4096, 4096) != 4LL * 4096 * 4096)
+        ++bad;
+    printf(bad ? "FAIL\n" : "OK\n");
+    return bad;
+}
+"""
+
+
+def test_header_compiles_as_c11_and_links(lib, tmp_path):
+    """A plain C11 program includes the header, links the library and reads
+    every status code's value and name through it."""
+    import shutil
+    import subprocess
+
+    from compensated_fp32_projection_gb300 import _native
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(_native.LIB_PATH)
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-L", libdir, "-l:libcompfp32.so", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "OK", out.stdout + out.stderr
 
 
 P = ctypes.c_void_p
@@ -149,10 +232,11 @@ def test_no_device_is_an_error_not_a_fallback(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     # valid arguments on a host without a usable sm_103 device: an error, never a CPU path
-    assert lib.comp_split_f32(P(4096), P(1 << 20), P(1 << 21), 8, None) == 2
-    assert lib.comp_gemm_f32x16(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, None) == 2
-    assert lib.comp_gemm_f16x2(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, None) == 2
-    assert lib.comp_gemm_f32x16_ws(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, P(1 << 26), 64, None) == 2
+    unsupported = STATUS_VALUES["COMP_ERR_UNSUPPORTED_DEVICE"]
+    assert lib.comp_split_f32(P(4096), P(1 << 20), P(1 << 21), 8, None) == unsupported
+    assert lib.comp_gemm_f32x16(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, None) == unsupported
+    assert lib.comp_gemm_f16x2(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, None) == unsupported
+    assert lib.comp_gemm_f32x16_ws(P(4096), P(1 << 20), P(1 << 24), 4, 4, 4, P(1 << 26), 64, None) == unsupported
 
 
 def test_package_import_does_not_need_the_library():

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-COMP_ERR_TIMEOUT = 4
+COMP_ERR_TIMEOUT = 5
 COMP_FAULT_CHECK_TIMEOUT = 0x0F01
 
 

@@ -42,6 +42,22 @@ def test_true_gemm_matches_numpy_matmul(orc):
         assert np.allclose(orc.gemm_den(x, W), den, rtol=1e-12, atol=0)
 
 
+def test_cast_gemm_matches_numpy_fp16_cast_then_matmul(orc):
+    # the single-FP16-cast product is numpy's round-to-nearest-even float16 cast
+    # of x (a library routine) times W in float64, rounded once to binary32; a
+    # cast that truncates or flushes subnormals, or a sum over the wrong
+    # operand, fails this by orders of magnitude more than the bound
+    for (M, N, K, s, scale) in [(9, 7, 5, 6, 1.0), (40, 24, 131, 7, 3.0), (16, 32, 520, 8, 1e-5)]:
+        x, W = _case(M, N, K, s, scale)
+        ref = x.astype(np.float16).astype(np.float64) @ _w64(W).T
+        den = np.abs(x.astype(np.float64)) @ np.abs(_w64(W)).T
+        y = orc.gemm_cast(x, W).astype(np.float64)
+        assert np.all(np.abs(y - ref) <= 2.0**-24 * np.abs(ref) + 1e-15 * den + 2.0**-149)
+        # and it is far from the compensated result wherever the cast loses bits
+        yc = orc.gemm_comp(x, W).astype(np.float64)
+        assert np.max(np.abs(y - yc) / (den + 1e-300)) > 1e-6
+
+
 def test_exact_fp16_inputs_all_products_coincide(orc):
     x, W = _case(40, 30, 77, 4)
     x = x.astype(np.float16).astype(np.float32)  # every x is exact in FP16, so lo = 0
