@@ -146,9 +146,7 @@ comp_status_t gemm_ws_impl(const float* x, const uint16_t* W, float* y, int64_t 
         uint16_t* hi = ws;
         uint16_t* lo = ws + M * Kp;
         uint16_t* wp = ws + 2 * M * Kp;
-        comp_status_t r = launch_split_padded(x, hi, lo, M, K, Kp, dev, s);
-        if (r == COMP_OK)
-            r = launch_pad_rows(W, wp, N, K, Kp, dev, s);
+        const comp_status_t r = launch_prep_padded(x, W, hi, lo, wp, M, N, K, Kp, dev, s);
         if (r != COMP_OK)
             return r;
         return launch_gemm_f16x2(hi, lo, wp, y, M, N, Kp, 0, dev, s, epi);

@@ -720,8 +720,12 @@ static_assert(128 * kCtrlRegs + 32 * kPromoters * kPromoRegs <= kThreads * kLaun
 // rows AR..127 read whatever follows inside the same stage, and since each
 // output row depends only on its own A row, those garbage rows only produce
 // outputs that are never stored.
-// KS: CTAs of a cluster that split K for the same tile (1: no split); their
-// partial sums are added in rank order through the leader's shared memory.
+// KS: CTAs of a cluster that split K for the same tile (1: no split).  With
+// AR = 32 their partial sums are added in rank order through the leader's
+// shared memory (rows 0..31 only); with AR = 128 every rank keeps its partial
+// tile in its own shared memory and reduces 1/KS of the tile's rows, reading
+// all ranks' partials through distributed shared memory and adding them in
+// rank order (reduce-scatter).
 template <int BN, int NS, int CH, int AR = BM, int KS = 1>
 struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
@@ -732,9 +736,12 @@ struct Cfg {
     static constexpr uint32_t kStageBytes = 2 * kPlaneBytes + kWBytes;  // hi | lo | W
     static_assert(kStageBytes % 1024 == 0, "stage alignment of the 128-byte swizzle");
     static_assert(kPlaneBytes + BM * BK * 2 <= kStageBytes, "the 128-row read of the lo plane stays in its stage");
-    static_assert(KS == 1 || (KS <= 8 && AR == 32), "split K serves problems of at most 32 rows");
-    static constexpr int kRedStride = BN / 2 + 4;  // floats per row of a reduction half (padded)
-    static constexpr uint32_t kRedBytes = KS > 1 ? 2u * 32u * kRedStride * 4u : 0u;
+    static_assert(KS == 1 || (KS <= 8 && AR == 32) || (AR == BM && (KS == 2 || KS == 4)), "split K");
+    static constexpr bool kScatter = KS > 1 && AR == BM;  // reduce-scatter of full 128-row tiles
+    static constexpr int kRedStride = kScatter ? BN + 4 : BN / 2 + 4;  // floats per buffer row (padded)
+    static constexpr uint32_t kRedBytes =
+        KS == 1 ? 0u : (kScatter ? static_cast<uint32_t>(BM) * kRedStride * 4u : 2u * 32u * kRedStride * 4u);
+    static_assert(!kScatter || (BN % 16 == 0 && (BM / KS) * (BN / 16) % 32 == 0), "reduce-scatter segments");
     static constexpr uint32_t kBarBytes = 512;
     static constexpr size_t kSmem = 1024 + NS * kStageBytes + kBarBytes + kRedBytes;
     static_assert(kSmem <= 232448, "shared memory");
@@ -751,6 +758,8 @@ struct Barriers {
     uint64_t drain;
     uint64_t red_full[2];  // leader: a peer's partial sums for one column half are in the buffer
     uint64_t red_go[2];    // peer: the leader's buffer for one column half is free for this peer
+    uint64_t rs_full;      // reduce-scatter: every rank's sums for this rank's rows are in its buffer
+    uint64_t rs_done;      // reduce-scatter: every rank has read the sums this rank sent it
     uint32_t tmem_base;
     int abort;
 };
@@ -766,9 +775,13 @@ constexpr uint32_t kFaultX2Reduce = 0x505;
 // The body of the single-CTA-tile product kernels.  With KS > 1 the CTAs of a
 // cluster of KS split K for the same tile: rank r takes the contiguous K blocks
 // [r nk / KS, (r + 1) nk / KS), and at the tile end the ranks' FP32 partial
-// sums are added in rank order in the leader (deterministic, no atomics, no
-// global scratch).  Split K is used for problems of at most 32 rows, whose
-// valid rows all sit in TMEM lanes 0..31 (promotion warps 4 and 8).
+// sums are added in rank order (deterministic, no atomics, no global scratch).
+// For problems of at most 32 rows (AR = 32), whose valid rows all sit in TMEM
+// lanes 0..31 (promotion warps 4 and 8), the peers send their sums to the
+// leader, which adds them.  For 128-row tiles (AR = 128) the ranks reduce the
+// tile between them (reduce-scatter through distributed shared memory): the
+// laya.cpp page's ordered reduction of split projection products (Vulkan
+// page, fused-build paragraph), here across the SMs of a cluster.
 template <int BN, int NS, int CH, int AR, int KS, bool EPI>
 __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, const CUtensorMap& tmap_lo,
                                                 const CUtensorMap& tmap_w, const Problem& P)
@@ -806,6 +819,8 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
             mbar_init(&bars->red_full[h], 1);
             mbar_init(&bars->red_go[h], 1);
         }
+        mbar_init(&bars->rs_full, x2::kPromoters);  // the warps of all ranks that hold this rank's rows
+        mbar_init(&bars->rs_done, KS * x2::kPromoters);
         bars->abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -1007,6 +1022,103 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
             }
             return true;
         };
+        // Reduce-scatter of one finished 128-row tile over the cluster (AR = 128):
+        // rank r owns rows [r 128/KS, (r+1) 128/KS) of the tile.  Every
+        // promotion warp stores its partial sums straight into the owner's
+        // receive buffer (slot of the sending rank; remote stores through
+        // distributed shared memory) and arrives on the owner's barrier; the
+        // owner's 256 promotion threads then add the KS slots of each element
+        // in rank order (binary32 RNE additions), apply the epilogue and store
+        // y in pieces of 16 columns.  Before a rank sends the next tile's sums,
+        // every owner has finished reading its buffer (rs_done).
+        auto scatter_tile = [&](int tt, int tile) -> bool {
+            auto wait_cluster = [&](uint64_t* bar, uint32_t parity) -> bool {
+                bool ok = true;
+                if (lane == 0) {
+                    const long long start = clock64();
+                    while (!mbar_try_wait_acquire_cluster(bar, parity)) {
+                        if (*reinterpret_cast<volatile int*>(&bars->abort) || clock64() - start > kWaitLimit) {
+                            atomicCAS(&g_fault_word, 0u, kFaultX2Reduce);
+                            *reinterpret_cast<volatile int*>(&bars->abort) = 1;
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (ok)
+                    (void)mbar_try_wait_acquire_cluster(bar, parity);
+                return ok;
+            };
+            constexpr int kRows = BM / KS;  // rows owned by one rank
+            if (tt > 0 && !wait_cluster(&bars->rs_done, static_cast<uint32_t>(tt - 1) & 1u))
+                return false;
+            {
+                const int row = wq * 32 + lane;           // this thread's row of the tile
+                const uint32_t owner = static_cast<uint32_t>(row / kRows);
+                const int slot_row = rank * kRows + row % kRows;  // receive buffer: [sender][row of the owner]
+                const uint32_t dst = mapa_shared(redbuf + slot_row * C::kRedStride + wh * C::kHalf, owner);
+#pragma unroll
+                for (int i = 0; i < C::kHalf; i += 4)
+                    st_cluster_v4(dst + 4u * i, R[i], R[i + 1], R[i + 2], R[i + 3]);
+                __syncwarp();
+                // the warp's 32 rows share one owner
+                if (lane == 0)
+                    mbar_arrive_release_cluster(mapa_shared(&bars->rs_full, owner));
+            }
+            if (!wait_cluster(&bars->rs_full, static_cast<uint32_t>(tt) & 1u))
+                return false;
+            constexpr int kSegsPerRow = BN / 16;
+            const int tid = (warp - 4) * 32 + lane;
+            const int64_t mt = static_cast<int64_t>(tile_m(tile, P)) * BM + rank * kRows;
+            const int64_t nt = static_cast<int64_t>(tile_n(tile, P)) * BN;
+            for (int sidx = tid; sidx < kRows * kSegsPerRow; sidx += 32 * x2::kPromoters) {
+                const int rl = sidx / kSegsPerRow;
+                const int c0 = (sidx % kSegsPerRow) * 16;
+                float acc[16];
+#pragma unroll
+                for (int p = 0; p < KS; ++p) {
+                    const float* src = redbuf + (p * kRows + rl) * C::kRedStride + c0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 v = *reinterpret_cast<const float4*>(src + 4 * q);
+                        if (p == 0) {
+                            acc[4 * q] = v.x;
+                            acc[4 * q + 1] = v.y;
+                            acc[4 * q + 2] = v.z;
+                            acc[4 * q + 3] = v.w;
+                        } else {
+                            acc[4 * q] = __fadd_rn(acc[4 * q], v.x);
+                            acc[4 * q + 1] = __fadd_rn(acc[4 * q + 1], v.y);
+                            acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], v.z);
+                            acc[4 * q + 3] = __fadd_rn(acc[4 * q + 3], v.w);
+                        }
+                    }
+                }
+                const int64_t m = mt + rl, n0 = nt + c0;
+                if (m < P.M && n0 < P.N) {
+                    if constexpr (EPI)
+                        epilogue16(acc, m, n0, P);
+                    float* yrow = P.y + m * P.N;
+                    if (P.vec_y && n0 + 16 <= P.N) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4*>(yrow + n0 + i) =
+                                make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (n0 + i < P.N)
+                                yrow[n0 + i] = acc[i];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                for (int p = 0; p < KS; ++p)
+                    mbar_arrive_release_cluster(mapa_shared(&bars->rs_done, static_cast<uint32_t>(p)));
+            return true;
+        };
         int g = 0, c = 0, kb = 0;
         int t = group;
         int tt = 0;  // tiles finished by this CTA
@@ -1041,13 +1153,17 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
             kb += n;
             if (kb == nkr) {
                 // tile finished: R holds this CTA's sums for y[m, nb .. nb + BN/2), m this thread's row
-                if (KS > 1 && wq == 0) {
+                if constexpr (C::kScatter) {
+                    // a failed wait leaves the abort flag raised; every promotion
+                    // warp then leaves at the next chunk's wait
+                    (void)scatter_tile(tt, t);
+                } else if (KS > 1 && wq == 0) {
                     // rows 0..31 (the only valid rows here) are in lane quarter 0.  A
                     // failed reduction leaves the abort flag raised; every promotion
                     // warp then leaves at the next chunk's wait, together.
                     (void)reduce_tile(tt);
                 }
-                if (KS == 1 || (rank == 0 && wq == 0)) {
+                if (!C::kScatter && (KS == 1 || (rank == 0 && wq == 0))) {
                     const int64_t m = static_cast<int64_t>(tile_m(t, P)) * BM + wq * 32 + lane;
                     const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
                     if (m < P.M && *reinterpret_cast<volatile int*>(&bars->abort) == 0) {
@@ -2597,7 +2713,9 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
         return bn == 224 ? launch_pair_bn<224, 4, 2>(th, tl, tw, ty, P, dev, stream)
                          : launch_pair_bn<256, 4, 2>(th, tl, tw, ty, P, dev, stream);
     }
-    // at most 32 rows and few tiles: split K over clusters of 2 or 4 CTAs
+    // few tiles: split K over clusters of 2 or 4 CTAs (at most 32 rows:
+    // 192-wide tiles reduced in the leader; otherwise 128 x 128 tiles reduced
+    // across the cluster)
     int ks = 1;
     if (M <= 32) {
         const int64_t t192 = (N + 191) / 192;
@@ -2605,8 +2723,14 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
             ks = 4;
         else if (t192 * 2 <= dev.sm_count && P.nk >= 8)
             ks = 2;
+    } else {
+        const int64_t t128 = ((M + BM - 1) / BM) * ((N + 127) / 128);
+        if (t128 * 4 <= dev.sm_count && P.nk >= 16)
+            ks = 4;
+        else if (t128 * 2 <= dev.sm_count && P.nk >= 8)
+            ks = 2;
     }
-    const int bn = ks > 1 ? 192 : pick_bn_x2(M, N, dev.sm_count);
+    const int bn = ks > 1 ? (M <= 32 ? 192 : 128) : pick_bn_x2(M, N, dev.sm_count);
     P.tiles_m = static_cast<int>((M + BM - 1) / BM);
     P.tiles_n = static_cast<int>((N + bn - 1) / bn);
     if (static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
@@ -2618,9 +2742,11 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn)))
         return COMP_ERR_CUDA;
     if (ks == 4)
-        return launch_x2_splitk<192, 6, 2, 32, 4>(th, tl, tw, P, dev, stream);
+        return M <= 32 ? launch_x2_splitk<192, 6, 2, 32, 4>(th, tl, tw, P, dev, stream)
+                       : launch_x2_splitk<128, 3, 2, BM, 4>(th, tl, tw, P, dev, stream);
     if (ks == 2)
-        return launch_x2_splitk<192, 6, 2, 32, 2>(th, tl, tw, P, dev, stream);
+        return M <= 32 ? launch_x2_splitk<192, 6, 2, 32, 2>(th, tl, tw, P, dev, stream)
+                       : launch_x2_splitk<128, 3, 2, BM, 2>(th, tl, tw, P, dev, stream);
     if (M <= 32) {
         if (bn == 192)
             return launch_x2_bn<192, 7, 2, 32>(th, tl, tw, P, dev, stream);
@@ -2637,7 +2763,12 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
 
 bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K)
 {
-    return M <= 32 && (N + swp::kTileN - 1) / swp::kTileN >= 32 && K % 8 == 0 && aligned16(x) && aligned16(W);
+    // W spans at least 32 tiles of 128 rows (the kernel streams W at the rate
+    // of the access pattern), or the K loop is at most 8 blocks of 64 (a short
+    // problem, where one launch beats the two-pass form's split and product)
+    const bool wide = (N + swp::kTileN - 1) / swp::kTileN >= 32;
+    const bool short_k = (K + BK - 1) / BK <= 8;
+    return M <= 32 && (wide || short_k) && K % 8 == 0 && aligned16(x) && aligned16(W);
 }
 
 comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
@@ -2756,3 +2887,4 @@ comp_status_t read_and_clear_fault(cudaStream_t stream, uint32_t* where)
 }
 
 }  // namespace compfp32
+

@@ -20,12 +20,11 @@ comp_status_t current_device(DeviceInfo* info);
 // Launchers (arguments already validated; sizes > 0).
 comp_status_t launch_split(const float* x, uint16_t* hi, uint16_t* lo, int64_t n, const DeviceInfo& dev,
                            cudaStream_t stream);
-// Split into planes [rows, Kp] (Kp >= K, a multiple of 8) with zero padding,
-// and a zero-padded copy of a binary16 matrix into rows of Kp elements.
-comp_status_t launch_split_padded(const float* x, uint16_t* hi, uint16_t* lo, int64_t rows, int64_t K, int64_t Kp,
-                                  const DeviceInfo& dev, cudaStream_t stream);
-comp_status_t launch_pad_rows(const uint16_t* src, uint16_t* dst, int64_t rows, int64_t K, int64_t Kp,
-                              const DeviceInfo& dev, cudaStream_t stream);
+// One launch: x [M, K] split into planes [M, Kp] (Kp >= K, a multiple of 8)
+// and W [N, K] copied into wp [N, Kp], all zero-padded past K.
+comp_status_t launch_prep_padded(const float* x, const uint16_t* W, uint16_t* hi, uint16_t* lo, uint16_t* wp,
+                                 int64_t M, int64_t N, int64_t K, int64_t Kp, const DeviceInfo& dev,
+                                 cudaStream_t stream);
 comp_status_t launch_geglu(const float* gate, const float* up, float* out, int64_t n, const DeviceInfo& dev,
                            cudaStream_t stream);
 comp_status_t launch_merge(const float* acc_hi, const float* acc_lo, float* y, int64_t n, const DeviceInfo& dev,
@@ -40,7 +39,8 @@ struct Epilogue {
 };
 
 // Fused split and swapped-operand product for at most 32 rows of x (K a
-// multiple of 8, x and W 16-byte aligned); preferred once N spans 32 tiles of 128.
+// multiple of 8, x and W 16-byte aligned); preferred once N spans 32 tiles of
+// 128, or when K is at most 8 blocks of 64.
 bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K);
 comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                 const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi = Epilogue{});

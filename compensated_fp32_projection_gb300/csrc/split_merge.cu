@@ -87,40 +87,53 @@ __global__ void __launch_bounds__(kThreads) split_scalar_kernel(const float* __r
     }
 }
 
-// Split of a row-major x [rows, K] into planes with a wider row stride Kp >= K
-// (a multiple of 8, so that their rows start on 16-byte boundaries); the
-// columns K..Kp-1 of both planes are +0, which adds exact zeros to every dot
-// product.  Any alignment of x.
-__global__ void __launch_bounds__(kThreads) split_pad_kernel(const float* __restrict__ x, uint16_t* __restrict__ hi,
-                                                             uint16_t* __restrict__ lo, int64_t rows, int64_t K,
-                                                             int64_t Kp)
+// The two-pass form's operands for any K: x [M, K] split into planes of row
+// stride Kp >= K (a multiple of 8, so that their rows start on 16-byte
+// boundaries), and W [N, K] copied into rows of Kp elements; columns K..Kp-1
+// are +0 in all three, which adds exact zeros to every dot product.  One
+// launch: block rows 0..M-1 split x, rows M..M+N-1 copy W.  Each thread
+// writes 8 consecutive elements of a row (16-byte stores), reading its
+// inputs with element loads (any alignment of x and W).
+__global__ void __launch_bounds__(kThreads) prep_padded_kernel(const float* __restrict__ x,
+                                                               const uint16_t* __restrict__ W,
+                                                               uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
+                                                               uint16_t* __restrict__ wp, int64_t M, int64_t N,
+                                                               int64_t K, int64_t Kp)
 {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t n = rows * Kp;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const int64_t r = i / Kp, k = i - r * Kp;
-        uint16_t h = 0, l = 0;
-        if (k < K) {
-            const float v = x[r * K + k];
-            const __half hh = __float2half_rn(v);
-            h = __half_as_ushort(hh);
-            l = __half_as_ushort(__float2half_rn(__fmul_rn(__fsub_rn(v, __half2float(hh)), 1024.0f)));
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t c8 = Kp / 8;  // 8-element pieces per row
+    for (int64_t r = blockIdx.x; r < M + N; r += gridDim.x) {
+        if (r < M) {
+            const float* xr = x + r * K;
+            for (int64_t c = threadIdx.x; c < c8; c += blockDim.x) {
+                const int64_t k0 = 8 * c;
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[e] = k0 + e < K ? xr[k0 + e] : 0.0f;
+                uint4 h, l;
+                split2(v[0], v[1], h.x, l.x);
+                split2(v[2], v[3], h.y, l.y);
+                split2(v[4], v[5], h.z, l.z);
+                split2(v[6], v[7], h.w, l.w);
+                *reinterpret_cast<uint4*>(hi + r * Kp + k0) = h;
+                *reinterpret_cast<uint4*>(lo + r * Kp + k0) = l;
+            }
+        } else {
+            const int64_t n = r - M;
+            const uint16_t* wr = W + n * K;
+            for (int64_t c = threadIdx.x; c < c8; c += blockDim.x) {
+                const int64_t k0 = 8 * c;
+                uint32_t h[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t a = k0 + 2 * e < K ? wr[k0 + 2 * e] : 0u;
+                    const uint32_t b = k0 + 2 * e + 1 < K ? wr[k0 + 2 * e + 1] : 0u;
+                    h[e] = a | (b << 16);
+                }
+                *reinterpret_cast<uint4*>(wp + n * Kp + k0) = make_uint4(h[0], h[1], h[2], h[3]);
+            }
         }
-        hi[i] = h;
-        lo[i] = l;
-    }
-}
-
-// Copy of a row-major binary16 matrix [rows, K] into rows of Kp >= K elements,
-// zero-filled past K.
-__global__ void __launch_bounds__(kThreads) pad_rows_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-                                                            int64_t rows, int64_t K, int64_t Kp)
-{
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t n = rows * Kp;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const int64_t r = i / Kp, k = i - r * Kp;
-        dst[i] = k < K ? src[r * K + k] : static_cast<uint16_t>(0);
     }
 }
 
@@ -201,17 +214,14 @@ comp_status_t launch_split(const float* x, uint16_t* hi, uint16_t* lo, int64_t n
     return COMP_OK;
 }
 
-comp_status_t launch_split_padded(const float* x, uint16_t* hi, uint16_t* lo, int64_t rows, int64_t K, int64_t Kp,
-                                  const DeviceInfo& dev, cudaStream_t stream)
+comp_status_t launch_prep_padded(const float* x, const uint16_t* W, uint16_t* hi, uint16_t* lo, uint16_t* wp,
+                                 int64_t M, int64_t N, int64_t K, int64_t Kp, const DeviceInfo& dev,
+                                 cudaStream_t stream)
 {
-    split_pad_kernel<<<grid_for(rows * Kp, dev), kThreads, 0, stream>>>(x, hi, lo, rows, K, Kp);
-    return launch_status();
-}
-
-comp_status_t launch_pad_rows(const uint16_t* src, uint16_t* dst, int64_t rows, int64_t K, int64_t Kp,
-                              const DeviceInfo& dev, cudaStream_t stream)
-{
-    pad_rows_kernel<<<grid_for(rows * Kp, dev), kThreads, 0, stream>>>(src, dst, rows, K, Kp);
+    const int64_t rows = M + N;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * kBlocksPerSm;
+    const unsigned grid = static_cast<unsigned>(rows < cap ? rows : cap);
+    prep_padded_kernel<<<grid, kThreads, 0, stream>>>(x, W, hi, lo, wp, M, N, K, Kp);
     return launch_status();
 }
 

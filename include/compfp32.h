@@ -118,9 +118,10 @@ comp_status_t comp_geglu_f32(const float* gate, const float* up, float* out, int
  *   x : [M, K] binary32 (input).   W : [N, K] binary16 (input).   y : [M, N] binary32 (output).
  * One kernel: x is split on the fly in shared memory, both products accumulate
  * in tensor memory, and the merge is the epilogue.  For at most 32 rows
- * against at least 32 * 128 rows of W (K a multiple of 8, x and W 16-byte
- * aligned) the kernel swaps the operands (y^T = W x^T, 128 rows of W per MMA)
- * and splits each K block of x into shared memory as it streams W.  For more
+ * against at least 32 * 128 rows of W, or with K at most 512 (K a multiple of
+ * 8, x and W 16-byte aligned), the kernel swaps the operands (y^T = W x^T,
+ * 128 rows of W per MMA) and splits each K block of x into shared memory as
+ * it streams W.  For more
  * than 128 rows, once the output fills about one wave of 128 x 192 tiles (same
  * operand conditions), a cluster of two CTAs computes each 256-row tile with
  * one instruction stream for both SMs' tensor cores; x arrives in FP32 and is
@@ -181,7 +182,8 @@ comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint
 /*
  * comp_gemm_f16x2_variant — comp_gemm_f16x2 with the kernel chosen by the
  * caller (testing and measurement): 0 automatic, 1 one CTA per 128-row tile
- * (with K split over clusters when M <= 32 and tiles are few), 2 pairs of CTAs
+ * (with K split over a cluster of 2 or 4 CTAs when the tiles are few; the
+ * partial sums are added in rank order, so reruns give identical bits), 2 pairs of CTAs
  * (one cluster, both SMs' tensor cores driven by one instruction stream) per
  * 256-row tile, 3 operands swapped (y^T = W x^T with 128 rows of W per tile;
  * M <= 32 only).  Same results within the same tolerance; a variant outside
@@ -212,9 +214,10 @@ int64_t comp_gemm_workspace_bytes_mnk(int64_t M, int64_t N, int64_t K);
  * (COMP_ERR_INVALID_VALUE); its contents are overwritten.  The call enqueues
  * the two-pass form: comp_split_f32 of x into the workspace, then
  * comp_gemm_f16x2.
- *   - M <= 32 against at least 32 * 128 rows of W, K a multiple of 8, x and W
- *     16-byte aligned: the fused swapped-operand kernel of comp_gemm_f32x16
- *     instead (faster there than split plus product); the workspace is unused.
+ *   - M <= 32 against at least 32 * 128 rows of W or with K <= 512, K a
+ *     multiple of 8, x and W 16-byte aligned: the fused swapped-operand kernel
+ *     of comp_gemm_f32x16 instead (one launch; faster there than split plus
+ *     product); the workspace is unused.
  *   - K a multiple of 8, W 16-byte aligned, workspace of at least
  *     comp_gemm_workspace_bytes(M, K): the planes [M, K] (hi, then lo) and
  *     the caller's W.

@@ -257,8 +257,12 @@ def test_device_status_clean(pkg):
 # CTA pairs per 256-row tile (2)
 # (16, 8000, 1024), (32, 1000, 520): at most 32 rows, K split over clusters of
 # 2 CTAs (the second with 9 K blocks, split 4 + 5); (32, 2048, 2048) and
-# (17, 260, 4096): clusters of 4
-SPLIT_K = [(16, 8000, 1024), (32, 1000, 520), (32, 2048, 2048)]
+# (17, 260, 4096): clusters of 4.  128-row tiles with K split over a cluster
+# and the tile reduced across it (reduce-scatter): (512, 1024, 1024) and
+# (129, 257, 4096), ragged, clusters of 4; (300, 500, 520) and
+# (1000, 776, 1032), clusters of 2 (9 and 17 K blocks: uneven ranges)
+SPLIT_K = [(16, 8000, 1024), (32, 1000, 520), (32, 2048, 2048), (512, 1024, 1024), (129, 257, 4096),
+           (300, 500, 520), (1000, 776, 1032)]
 
 
 @pytest.mark.parametrize("shape", SHAPES + SPLIT_K + [(2048, 2048, 256), (2000, 2001, 136), (300, 4096, 64)],
@@ -316,7 +320,8 @@ def test_swapped_operands_full(pkg, orc, shape):
 
 @pytest.mark.parametrize("shape", SPLIT_K, ids=lambda s: "x".join(map(str, s)))
 def test_split_k_deterministic(pkg, shape):
-    # the partial sums of the K ranges are added in a fixed order: bit-identical reruns
+    # the partial sums of the K ranges are added in a fixed order: bit-identical
+    # reruns (a reduction in arrival order would differ between runs)
     from compensated_fp32_projection_gb300 import workloads
 
     M, N, K = shape
