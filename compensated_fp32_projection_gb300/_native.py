@@ -39,6 +39,7 @@ SIGNATURES = {
     "comp_gemm_f32x16_noalloc": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "comp_device_status": (_int, [_vp, ctypes.POINTER(_u32)]),
     "comp_check_wait_timeout": (_int, [_vp]),
+    "comp_check_stalled_pipeline": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "comp_status_string": (ctypes.c_char_p, [_int]),
     "comp_version": (_int, []),
 }

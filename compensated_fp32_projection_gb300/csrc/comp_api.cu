@@ -337,6 +337,24 @@ comp_status_t comp_gemm_f16x2_epilogue(const uint16_t* hi, const uint16_t* lo, c
 
 
 
+comp_status_t comp_check_stalled_pipeline(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y,
+                                          int64_t M, int64_t N, int64_t K, int variant, comp_stream_t stream)
+{
+    DeviceInfo dev;
+    bool empty;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (variant != 2 && variant != 3)
+        return COMP_ERR_INVALID_VALUE;
+    if (variant == 3 && M > 32)
+        return COMP_ERR_INVALID_VALUE;
+    const comp_status_t st = check_gemm(hi, 2, W, y, M, N, K, s, &dev, &empty);
+    if (st != COMP_OK || empty)
+        return st;
+    if (!lo || overlap(y, 4 * M * N, lo, 2 * M * K) || !gemm_f16x2_supported(hi, lo, W, K))
+        return COMP_ERR_INVALID_VALUE;
+    return launch_gemm_f16x2(hi, lo, W, y, M, N, K, variant, dev, s, Epilogue{}, true);
+}
+
 comp_status_t comp_check_wait_timeout(comp_stream_t stream)
 {
     DeviceInfo dev;

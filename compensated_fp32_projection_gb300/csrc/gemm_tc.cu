@@ -304,6 +304,7 @@ struct Problem {
     int tma_y;                     // y is written with tensor-map stores (kernels that support it)
     const float* bias = nullptr;   // epilogue: [N], added to y (nullptr: none)
     const float* gate = nullptr;   // epilogue: [M, N], y times gelu(gate) (nullptr: factor 1)
+    int stall = 0;                 // diagnostic: the producer leaves out its first stage's loads
 };
 
 // Epilogue of a GEGLU feed-forward step (laya.cpp docs/vulkan.md, feed-forward
@@ -1634,9 +1635,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                 const uint32_t fb = full0 + static_cast<uint32_t>(s) * 8u;
                 if (leader_cta)
                     mbar_arrive_expect_tx(&bars->full[s], C::kTxBytes);
-                tma_load_2d_pair(st, &tmap_hi, fb, k0, m0);
-                tma_load_2d_pair(st + pair::kPlaneBytes, &tmap_lo, fb, k0, m0);
-                tma_load_2d_pair(st + 2 * pair::kPlaneBytes, &tmap_w, fb, k0, n0);
+                // diagnostic (comp_check_stalled_pipeline): the leader's first
+                // stage never lands, so the MMA warp's bounded wait gives up
+                if (!(P.stall && leader_cta && g == 0)) {
+                    tma_load_2d_pair(st, &tmap_hi, fb, k0, m0);
+                    tma_load_2d_pair(st + pair::kPlaneBytes, &tmap_lo, fb, k0, m0);
+                    tma_load_2d_pair(st + 2 * pair::kPlaneBytes, &tmap_w, fb, k0, n0);
+                }
                 issued = g + 1;
                 if (++kb == P.nk) {
                     kb = 0;
@@ -2033,7 +2038,9 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
                     tma_load_2d(st + C::kXFOff + i * C::kXF, &tmap_hi, &bars->xfull[s], (kb0 + i) * BK, 0);
             }
             mbar_arrive_expect_tx(&bars->full[s], n * (C::kWBox + (FX ? 0u : 2 * C::kXBox)));
-            for (int i = 0; i < n; ++i)
+            // diagnostic (comp_check_stalled_pipeline): the first stage's W never
+            // lands, so the MMA warp's bounded wait gives up
+            for (int i = 0; i < n && !(P.stall && g == 0); ++i)
                 tma_load_2d(st + i * C::kWBox, &tmap_w, &bars->full[s], (kb0 + i) * BK, t * swp::kTileN);
             for (int i = 0; i < n && !FX; ++i) {  // rows >= M read as 0
                 uint8_t* xb = st + BPS * C::kWBox + i * 2 * C::kXBox;
@@ -2654,7 +2661,7 @@ bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t
 
 comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
                                 int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream,
-                                const Epilogue& epi)
+                                const Epilogue& epi, bool stall)
 {
     if (!gemm_f16x2_supported(hi, lo, W, K) || variant < 0 || variant > 3 || (variant == 3 && M > 32))
         return COMP_ERR_INVALID_VALUE;
@@ -2673,6 +2680,7 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     P.tma_y = 0;
     P.bias = epi.bias;
     P.gate = epi.gate;
+    P.stall = stall ? 1 : 0;
     CUtensorMap th{}, tl{}, tw{};
     // at most 32 rows and at least 32 tiles of 128 columns: operands swapped,
     // W streams through full 128-row MMAs

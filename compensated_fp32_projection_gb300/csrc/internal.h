@@ -61,9 +61,12 @@ comp_status_t launch_gemm_tc(const float* x, const uint16_t* W, float* y, int64_
 bool gemm_f16x2_supported(const void* hi, const void* lo, const void* W, int64_t K);
 // variant: 0 automatic, 1 one CTA per 128-row tile, 2 CTA pairs on 256-row
 // tiles, 3 operands swapped (M <= 32).
+// stall: diagnostic run of the CTA-pair (variant 2) or swapped (variant 3)
+// kernel whose producer leaves out its first stage's loads (see
+// comp_check_stalled_pipeline).
 comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
                                 int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream,
-                                const Epilogue& epi = Epilogue{});
+                                const Epilogue& epi = Epilogue{}, bool stall = false);
 
 // One thread runs a bounded wait that cannot succeed (comp_check_wait_timeout).
 comp_status_t launch_check_wait_timeout(cudaStream_t stream);

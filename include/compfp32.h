@@ -330,6 +330,25 @@ comp_status_t comp_device_status(comp_stream_t stream, uint32_t* where);
 #define COMP_FAULT_CHECK_TIMEOUT 0x0F01u
 comp_status_t comp_check_wait_timeout(comp_stream_t stream);
 
+/*
+ * comp_check_stalled_pipeline — diagnostic of the same reporting inside the
+ * real kernels.  Enqueues comp_gemm_f16x2_variant(hi, lo, W, y, M, N, K,
+ * variant) for variant 2 (CTA pairs) or 3 (operands swapped; M <= 32),
+ * except that the kernel's producer leaves out the loads of
+ * its first pipeline stage.  The MMA warp's bounded wait for that stage gives
+ * up after about a second and raises the abort flag; every role then leaves
+ * its loop, the issued loads and MMAs are waited for (bounded) and tensor
+ * memory is freed.  comp_device_status then returns COMP_ERR_TIMEOUT with one
+ * of the kernel's fault codes (0x701 to 0x703 for pairs, 0x801 to 0x804 for
+ * the swapped kernel), and the context stays usable.  y is left undefined.
+ * The pages have no counterpart; the call exists so that the abort path of
+ * the pipelined kernels can be tested without faulting or hanging a GPU.
+ * Errors: those of comp_gemm_f16x2_variant, and COMP_ERR_INVALID_VALUE for
+ * another variant or a shape the variant does not take.
+ */
+comp_status_t comp_check_stalled_pipeline(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y,
+                                          int64_t M, int64_t N, int64_t K, int variant, comp_stream_t stream);
+
 /* Human-readable name of a status code (a static string). */
 const char* comp_status_string(comp_status_t status);
 
