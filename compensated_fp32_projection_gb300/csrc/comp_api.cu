@@ -160,7 +160,7 @@ comp_status_t gemm_f16x2_impl(const uint16_t* hi, const uint16_t* lo, const uint
     DeviceInfo dev;
     bool empty;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (variant < 0 || variant > 3 || (variant == 3 && M > 32))
+    if (variant < 0 || variant > 4 || (variant == 3 && M > 32))
         return COMP_ERR_INVALID_VALUE;
     const comp_status_t st = check_gemm(hi, 2, W, y, M, N, K, s, &dev, &empty);
     if (st != COMP_OK || empty)

@@ -714,7 +714,9 @@ constexpr int kCtrlRegs = 40;
 constexpr int kPromoRegs = 232;
 static_assert(128 * kCtrlRegs + 32 * kPromoters * kPromoRegs <= kThreads * kLaunchRegs, "register split");
 // BN: tile width; NS: pipeline stages; CH: K blocks per accumulation chunk
-// (tensor-core accumulation restarts every CH * 64 of K); AR: rows of the hi
+// (tensor-core accumulation restarts every CH * 64 of K; CH = 0 is the
+// measurement option of one tensor-core chain per product over all of K, hi
+// and lo in separate accumulators merged once at the tile end); AR: rows of the hi
 // and lo boxes.  AR < 128 serves problems of at most AR rows: only AR rows of
 // each plane are loaded, so a stage is small and many stages stay in flight
 // while W streams.  The MMA still reads 128 rows from each plane's offset;
@@ -730,7 +732,8 @@ static_assert(128 * kCtrlRegs + 32 * kPromoters * kPromoRegs <= kThreads * kLaun
 template <int BN, int NS, int CH, int AR = BM, int KS = 1>
 struct Cfg {
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
-    static_assert(NS >= 2 && CH >= 1 && CH <= NS, "stages");
+    static_assert(NS >= 2 && CH >= 0 && CH <= NS, "stages");
+    static_assert(CH > 0 || (KS == 1 && 2 * BN <= 512), "one chain per product: two accumulators, no split K");
     static_assert(AR == BM || AR == 32, "box rows");
     static constexpr uint32_t kPlaneBytes = AR * BK * 2;  // an AR x 64 FP16 box
     static constexpr uint32_t kWBytes = BN * BK * 2;
@@ -867,6 +870,48 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
             if (*reinterpret_cast<volatile int*>(&bars->abort))
                 for (int g = issued - NS < 0 ? 0 : issued - NS; g < issued; ++g)
                     drain_wait(&bars->full[g % NS], (g / NS) & 1);
+        } else if (warp == 1 && CH == 0) {
+            // ---------------- MMA issuer, one tensor-core chain per product (CH = 0) ----------------
+            // hi * W^T into columns [0, BN), lo * W^T into [BN, 2 BN), over all K
+            // blocks of the tile; the promotion warps merge them once at the
+            // tile end and hand the accumulators back before the next tile.
+            const uint32_t leader = lane == 0 ? 1u : 0u;
+            const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
+            int tt = 0;
+            bool ok = true;
+            for (int g = 0; g < total; ++g) {
+                const int s = g % NS;
+                const int kbi = g % nkr;
+                bool r = true;
+                if (lane == 0) {
+                    if (kbi == 0 && tt > 0)
+                        r = wait_bounded(&bars->dfree[0], (tt - 1) & 1, &bars->abort, kFaultX2MmaFree);
+                    r = r && wait_bounded(&bars->full[s], (g / NS) & 1, &bars->abort, kFaultX2MmaFull);
+                }
+                ok = __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint64_t st = desc0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+                const uint64_t a_hi = st, a_lo = st + (C::kPlaneBytes >> 4), w = st + ((2 * C::kPlaneBytes) >> 4);
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)
+                    umma_f16_by(leader, tmem + BN, a_lo + 2 * j, w + 2 * j, C::kIdesc, (kbi > 0 || j > 0) ? 1u : 0u);
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)
+                    umma_f16_by(leader, tmem, a_hi + 2 * j, w + 2 * j, C::kIdesc, (kbi > 0 || j > 0) ? 1u : 0u);
+                umma_commit_by(leader, &bars->empty[s]);
+                if (kbi == nkr - 1) {
+                    umma_commit_by(leader, &bars->dfull[0]);
+                    ++tt;
+                }
+            }
+            if (!ok) {
+                umma_commit_by(leader, &bars->drain);
+                if (lane == 0)
+                    drain_wait(&bars->drain, 0);
+                __syncwarp();
+            }
         } else if (warp == 1) {
             // ---------------- MMA issuer, one chunk of CH K blocks at a time ----------------
             // The whole warp runs the loop, so descriptors are warp-uniform;
@@ -950,6 +995,50 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
                 if (lane == 0)
                     drain_wait(&bars->drain, 0);
                 __syncwarp();
+            }
+        }
+    } else if (CH == 0) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(x2::kPromoRegs));
+        // ---------------- promotion, one chain per product: y = D_hi + 2^-10 D_lo per tile ----------------
+        const int wq = warp & 3;
+        const int wh = (warp - 4) >> 2;
+        int t = group;
+        for (int g0 = 0, tt = 0; g0 < total; g0 += nkr, ++tt, t += groups) {
+            if (warp == 4)
+                (void)lane0_wait(&bars->dfull[0], tt & 1, &bars->abort, kFaultX2Promote);
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * x2::kPromoters) : "memory");
+            if (*reinterpret_cast<volatile int*>(&bars->abort))
+                break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + wh * C::kHalf;
+            float R[C::kHalf];
+#pragma unroll
+            for (int c0 = 0; c0 < C::kHalf; c0 += 16) {
+                uint32_t vh[16], vl[16];
+                tmem_ld16(taddr + c0, vh);
+                tmem_ld16(taddr + BN + c0, vl);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    R[c0 + i] = __fadd_rn(__uint_as_float(vh[i]), __fmul_rn(__uint_as_float(vl[i]), 0x1p-10f));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars->dfree[0]);
+            const int64_t m = static_cast<int64_t>(tile_m(t, P)) * BM + wq * 32 + lane;
+            const int64_t nb = static_cast<int64_t>(tile_n(t, P)) * BN + wh * C::kHalf;
+            if (m < P.M) {
+                if constexpr (EPI) {
+#pragma unroll
+                    for (int p = 0; p < C::kHalf; p += 16)
+                        epilogue16(R + p, m, nb + p, P);
+                }
+                float* yrow = P.y + m * P.N;
+#pragma unroll
+                for (int i = 0; i < C::kHalf; ++i)
+                    if (nb + i < P.N)
+                        yrow[nb + i] = R[i];
             }
         }
     } else {
@@ -2663,7 +2752,7 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
                                 int64_t N, int64_t K, int variant, const DeviceInfo& dev, cudaStream_t stream,
                                 const Epilogue& epi, bool stall)
 {
-    if (!gemm_f16x2_supported(hi, lo, W, K) || variant < 0 || variant > 3 || (variant == 3 && M > 32))
+    if (!gemm_f16x2_supported(hi, lo, W, K) || variant < 0 || variant > 4 || (variant == 3 && M > 32))
         return COMP_ERR_INVALID_VALUE;
     // CTA pairs once the output fills about one wave of single-CTA tiles: below
     // that, pipeline fill dominates and the 128-row tiles spread over more SMs.
@@ -2701,6 +2790,19 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
         // hence the same chunks: both forms give identical bits.
         return mp == 16 ? launch_swap<16, 2, 5>(th, tl, tw, P, dev, stream)
                         : launch_swap<32, 2, 4>(th, tl, tw, P, dev, stream);
+    }
+    if (variant == 4) {
+        // measurement option: one tensor-core chain per product over all of K,
+        // one CTA per 128 x 128 tile
+        P.tiles_m = static_cast<int>((M + BM - 1) / BM);
+        P.tiles_n = static_cast<int>((N + 127) / 128);
+        if (static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
+            return COMP_ERR_INVALID_VALUE;
+        if (!encode_2d(&th, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hi, K, M, BK, BM) ||
+            !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, BM) ||
+            !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, 128))
+            return COMP_ERR_CUDA;
+        return launch_x2_bn<128, 4, 0>(th, tl, tw, P, dev, stream);
     }
     if (pairs) {
         // CTA pairs on 256-row tiles

@@ -186,8 +186,15 @@ comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint
  * partial sums are added in rank order, so reruns give identical bits), 2 pairs of CTAs
  * (one cluster, both SMs' tensor cores driven by one instruction stream) per
  * 256-row tile, 3 operands swapped (y^T = W x^T with 128 rows of W per tile;
- * M <= 32 only).  Same results within the same tolerance; a variant outside
- * 0..3, or 3 with M > 32, is COMP_ERR_INVALID_VALUE.
+ * M <= 32 only), 4 one tensor-core chain per product over all of K (hi and lo
+ * in separate FP32 accumulators, merged once at the tile end; one CTA per
+ * 128 x 128 tile).  Variant 4 exists to measure what the chunked promotion of
+ * the other kernels buys (laya.cpp docs/vulkan.md, AMD accumulation
+ * paragraph: separate FP32 additions of partial results against one long
+ * chain); it is slower, and its error grows with K: at K = 16384 it no longer
+ * meets the 100x gain over a single FP16 cast that the other variants meet.
+ * Variants 0..3 give the same results within the same tolerance; a variant
+ * outside 0..4, or 3 with M > 32, is COMP_ERR_INVALID_VALUE.
  */
 comp_status_t comp_gemm_f16x2_variant(const uint16_t* hi, const uint16_t* lo, const uint16_t* W, float* y, int64_t M,
                                       int64_t N, int64_t K, int variant, comp_stream_t stream);

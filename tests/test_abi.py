@@ -180,7 +180,7 @@ def test_two_pass_argument_errors(lib):
     assert f2(P(4096), P(1 << 16), P(1 << 20), P(4096 + 32), 4, 4, 8, None) == 1  # y overlaps hi
     assert f2(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 1 << 40, 1 << 40, 8, None) == 1
     assert f2(None, None, None, None, 0, 4, 8, None) == 0
-    assert lib.comp_gemm_f16x2_variant(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, 4, None) == 1
+    assert lib.comp_gemm_f16x2_variant(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, 5, None) == 1
     assert lib.comp_gemm_f16x2_variant(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 33, 4, 8, 3, None) == 1
     assert lib.comp_gemm_f16x2_variant(P(4096), P(1 << 16), P(1 << 20), P(1 << 24), 4, 4, 8, -1, None) == 1
     # comp_gemm_f32x16_ws(x, W, y, M, N, K, workspace, bytes, stream)
@@ -198,7 +198,7 @@ def test_epilogue_argument_errors(lib):
     assert ep(None, None, None, None, None, 0, 8, 8, None, 0, None) == 0  # empty output: no-op
     # comp_gemm_f16x2_epilogue(hi, lo, W, bias, gate, y, M, N, K, variant, stream)
     assert e2(P(4096), P(1 << 16), P(1 << 20), P(y + 28), None, P(y), 4, 8, 8, 0, None) == 1
-    assert e2(P(4096), P(1 << 16), P(1 << 20), None, None, P(y), 4, 8, 8, 4, None) == 1  # variant out of range
+    assert e2(P(4096), P(1 << 16), P(1 << 20), None, None, P(y), 4, 8, 8, 5, None) == 1  # variant out of range
 
 
 def test_geglu_argument_errors(lib):

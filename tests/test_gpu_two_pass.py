@@ -298,7 +298,7 @@ def test_product_variant_out_of_range(pkg):
 
     h = torch.zeros(8, 64, dtype=torch.float16, device="cuda")
     with pytest.raises(CompError):
-        pkg.comp_gemm_f16x2_variant(h, h.clone(), torch.zeros(16, 64, dtype=torch.float16, device="cuda"), 4)
+        pkg.comp_gemm_f16x2_variant(h, h.clone(), torch.zeros(16, 64, dtype=torch.float16, device="cuda"), 5)
     h40 = torch.zeros(40, 64, dtype=torch.float16, device="cuda")
     with pytest.raises(CompError):  # swapped operands need M <= 32
         pkg.comp_gemm_f16x2_variant(h40, h40.clone(), torch.zeros(16, 64, dtype=torch.float16, device="cuda"), 3)
