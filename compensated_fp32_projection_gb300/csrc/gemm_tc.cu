@@ -1402,35 +1402,154 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t par
 }
 
 // Descriptor offset, in 16-byte units from the stage base, of K slice j
-// (16 of K) of the hi or lo operand of a stage.  Planes: the hi box (128 rows
-// of 64 FP16, 128 bytes each), then the lo box.  Fused kernel:
-// line r of box h (h = 0, 1) holds the hi values of K 32h .. 32h+31 of row r
-// in its first 64 bytes and their lo values in its last 64 bytes.  Both are
-// 128-byte rows with the 128-byte swizzle, so one descriptor form serves.
-template <bool FUSED>
-__device__ __forceinline__ constexpr uint32_t a_slice(int j, bool lo)
+// (16 of K) of the hi or lo operand of a stage of the fused kernel: line r of
+// box h (h = 0, 1) holds the hi values of K 32h .. 32h+31 of row r in its
+// first 64 bytes and their lo values in its last 64 bytes, 128-byte rows with
+// the 128-byte swizzle like the planes' boxes.
+__device__ __forceinline__ constexpr uint32_t fused_a_slice(int j, bool lo)
 {
-    return FUSED ? static_cast<uint32_t>((j >> 1) * (pair::kPlaneBytes >> 4) + (lo ? 4 : 0) + 2 * (j & 1))
-                 : static_cast<uint32_t>((lo ? (pair::kPlaneBytes >> 4) : 0) + 2 * j);
+    return static_cast<uint32_t>((j >> 1) * (pair::kPlaneBytes >> 4) + (lo ? 4 : 0) + 2 * (j & 1));
 }
 
-// The MMA issuer of a CTA pair (leader CTA, the whole warp runs the loop,
-// lane 0 waits and issues), one chunk of CH K blocks at a time: lo * W^T of
-// the chunk into a fresh accumulator, then hi * W^T, whose first MMA scales
-// the accumulator by 2^-10 on input.  Stage s holds, in both CTAs, the hi and
-// lo values of the CTA's 128 rows (first 32 KB, laid out as a_slice<FUSED>
-// says) and the CTA's half of the W rows.
-//   Two-pass product: bars->full[s] (leader) completes when all of them have
-// landed; a chunk starts once all its stages are in.
-//   Fused kernel: bars->full[s] counts the W bytes and split[s] the split
-// warps of both CTAs (the other CTA's after a shared-memory release at
-// cluster scope: relaxed polls at cluster scope, then the acquire fence).  A
-// chunk starts once its first stage is ready, and each later stage is waited
-// for just before its first MMA, so the products of a stage overlap the split
-// of the next.
-template <int BN, int NS, int CH, bool FUSED>
-__device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint64_t* split, uint8_t* smem, uint32_t tmem,
-                                              int total, const Problem& P, int lane)
+// The MMA issuer of the two-pass pair product (leader CTA; the whole warp
+// runs the loop, lane 0 waits and issues), one chunk of CH K blocks at a
+// time: lo * W^T of the chunk into a fresh accumulator, then hi * W^T, whose
+// first MMA scales the accumulator by 2^-10 on input.  Stage s holds, in both
+// CTAs, the CTA's 128 rows of the hi plane (16 KB), then of the lo plane, then
+// its half of the W rows; bars->full[s] (leader) completes when both CTAs'
+// boxes have landed, and a chunk starts once all its stages are in.
+//   This thread's work between MMAs decides the pace: the tensor pipe takes
+// 112 cycles per 256 x 224 x 16 pair MMA, and issuing one takes the thread
+// 60 to 80 cycles.  So the loop keeps its bookkeeping short: the stage,
+// full-barrier parity and descriptor words of a chunk advance by additions
+// (no division), descriptors are 32-bit words, and the barrier tests for the
+// next chunk run in the window where the first hi MMA waits for the lo
+// products to finish accumulating, with the three tests issued together.
+template <int BN, int NS, int CH>
+__device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint8_t* smem, uint32_t tmem, int total,
+                                              const Problem& P, int lane)
+{
+    using C = pair::Cfg<BN, NS, CH>;
+    const uint32_t leader = lane == 0 ? 1u : 0u;
+    const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
+    const uint32_t dlo0 = static_cast<uint32_t>(desc0);
+    const uint32_t dhi = static_cast<uint32_t>(desc0 >> 32);
+    constexpr uint32_t kSW = C::kStageBytes >> 4;     // one stage, in descriptor units
+    constexpr uint32_t kPW = pair::kPlaneBytes >> 4;  // one plane box
+    const int nk = P.nk;
+    // stage and full-barrier parity of block i of a chunk whose first block
+    // sits at stage s with parity ph (CH <= NS: the ring wraps at most once)
+    auto stage_of = [](int s, uint32_t ph, int i, int& si, uint32_t& pi) {
+        si = s + i;
+        pi = ph;
+        if (si >= NS) {
+            si -= NS;
+            pi ^= 1u;
+        }
+    };
+    auto test_chunk = [&](int s, uint32_t ph, int c, int n) -> bool {
+        uint32_t r = (c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1)) ? 1u : 0u;
+#pragma unroll
+        for (int i = 0; i < CH; ++i)
+            if (i < n) {
+                int si;
+                uint32_t pi;
+                stage_of(s, ph, i, si, pi);
+                r &= mbar_test_wait(&bars->full[si], pi) ? 1u : 0u;
+            }
+        return r != 0;
+    };
+    auto wait_chunk = [&](int s, uint32_t ph, int c, int n) -> bool {
+        bool ok = true;
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+                if (ok && i < n) {
+                    int si;
+                    uint32_t pi;
+                    stage_of(s, ph, i, si, pi);
+                    ok = wait_bounded(&bars->full[si], pi, &bars->abort, kFaultPairMma);
+                }
+            if (ok && c >= 2)
+                ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort, kFaultPairMma);
+        }
+        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    };
+    // chunk c starts at block g (block kb of its tile), stage s, parity ph, and has n blocks
+    int g = 0, c = 0, kb = 0, s = 0;
+    uint32_t ph = 0;
+    int n = nk < CH ? nk : CH;
+    bool ok = total == 0 || wait_chunk(s, ph, c, n);
+    while (g < total && ok) {
+        const uint32_t d = tmem + (c & 1) * BN;
+        tc_fence_after();
+        uint32_t st[CH];  // descriptor word of each stage of the chunk
+        int sidx[CH];
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+            uint32_t pi;
+            stage_of(s, ph, i, sidx[i], pi);
+            st[i] = dlo0 + static_cast<uint32_t>(sidx[i]) * kSW;
+        }
+#pragma unroll
+        for (int i = 0; i < CH; ++i)  // lo * W^T of the chunk; the very first overwrites D
+            if (i < n) {
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)
+                    umma_pair_w_by(leader, d, st[i] + kPW + 2 * j, st[i] + 2 * kPW + 2 * j, dhi, C::kIdesc,
+                                   (i > 0 || j > 0) ? 1u : 0u);
+            }
+        // the next chunk, and whether its stages and accumulator are ready
+        const int g2 = g + n, c2 = c + 1;
+        int kb2 = kb + n;
+        if (kb2 == nk)
+            kb2 = 0;
+        const int n2 = nk - kb2 < CH ? nk - kb2 : CH;
+        int s2;
+        uint32_t ph2;
+        stage_of(s, ph, n, s2, ph2);
+        const bool ready2 = g2 >= total || test_chunk(s2, ph2, c2, n2);
+#pragma unroll
+        for (int i = 0; i < CH; ++i)  // hi * W^T; the first scales D by 2^-10 on input
+            if (i < n) {
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j) {
+                    if (i == 0 && j == 0)
+                        umma_pair_w_scale10_by(leader, d, st[0], st[0] + 2 * kPW, dhi, C::kIdesc);
+                    else
+                        umma_pair_w_by(leader, d, st[i] + 2 * j, st[i] + 2 * kPW + 2 * j, dhi, C::kIdesc, 1u);
+                }
+                umma_commit_pair_by(leader, &bars->empty[sidx[i]], 0x3);
+            }
+        umma_commit_pair_by(leader, &bars->dfull[c & 1], 0x3);
+        g = g2;
+        c = c2;
+        kb = kb2;
+        n = n2;
+        s = s2;
+        ph = ph2;
+        if (g < total && !ready2)
+            ok = wait_chunk(s, ph, c, n);
+    }
+    if (!ok) {
+        umma_commit_pair_by(leader, &bars->drain, 0x1);
+        if (lane == 0)
+            drain_wait(&bars->drain, 0);
+        __syncwarp();
+    }
+}
+
+// The MMA issuer of the fused pair kernel, in the same chunk order.  Stage s
+// holds, in both CTAs, hi and lo of the CTA's 128 rows (first 32 KB, laid
+// out as fused_a_slice says) and the CTA's half of the W rows.
+// bars->full[s] counts the W bytes and split[s] the split warps of both CTAs
+// (the other CTA's after a shared-memory release at cluster scope: relaxed
+// polls at cluster scope, then the acquire fence).  A chunk starts once its
+// first stage is ready, and each later stage is waited for just before its
+// first MMA, so the products of a stage overlap the split of the next.
+template <int BN, int NS, int CH>
+__device__ __forceinline__ void pair_mma_role_fused(pair::Barriers* bars, uint64_t* split, uint8_t* smem,
+                                                    uint32_t tmem, int total, const Problem& P, int lane)
 {
     using C = pair::Cfg<BN, NS, CH>;
     const uint32_t leader = lane == 0 ? 1u : 0u;
@@ -1438,39 +1557,24 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint64_t* sp
     auto test_stage = [&](int g) -> bool {
         const int s = g % NS;
         const uint32_t par = (g / NS) & 1;
-        if constexpr (FUSED) {
-            if (!(mbar_test_wait(&bars->full[s], par) && mbar_test_wait_relaxed_cluster(&split[s], par)))
-                return false;
-            fence_acquire_smem_cluster();
-            return true;
-        } else {
-            return mbar_test_wait(&bars->full[s], par);
-        }
+        if (!(mbar_test_wait(&bars->full[s], par) && mbar_test_wait_relaxed_cluster(&split[s], par)))
+            return false;
+        fence_acquire_smem_cluster();
+        return true;
     };
     auto wait_stage = [&](int g) -> bool {  // lane 0
         const int s = g % NS;
         const uint32_t par = (g / NS) & 1;
-        bool ok = wait_bounded(&bars->full[s], par, &bars->abort, kFaultPairMma);
-        if constexpr (FUSED)
-            ok = ok && wait_bounded_cluster(&split[s], par, &bars->abort, kFaultPairMma);
-        return ok;
+        return wait_bounded(&bars->full[s], par, &bars->abort, kFaultPairMma) &&
+               wait_bounded_cluster(&split[s], par, &bars->abort, kFaultPairMma);
     };
-    constexpr int kFirst = FUSED ? 1 : CH;  // stages a chunk waits for before its first MMA
-    auto test_chunk = [&](int g, int c, int n) -> bool {
-        bool r = c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1);
-#pragma unroll
-        for (int i = 0; i < kFirst; ++i)
-            if (i < n)
-                r = r && test_stage(g + i);
-        return r;
+    auto test_chunk = [&](int g, int c) -> bool {
+        return (c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1)) && test_stage(g);
     };
-    auto wait_chunk = [&](int g, int c, int n) -> bool {
+    auto wait_chunk = [&](int g, int c) -> bool {
         bool ok = true;
         if (lane == 0) {
-#pragma unroll
-            for (int i = 0; i < kFirst; ++i)
-                if (ok && i < n)
-                    ok = wait_stage(g + i);
+            ok = wait_stage(g);
             if (ok && c >= 2)
                 ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort, kFaultPairMma);
         }
@@ -1478,7 +1582,7 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint64_t* sp
     };
     int g = 0, c = 0, kb = 0;
     int n = (P.nk < CH) ? P.nk : CH;
-    bool ok = total == 0 || wait_chunk(0, 0, n);
+    bool ok = total == 0 || wait_chunk(0, 0);
     while (g < total && ok) {
         const int b = c & 1;
         tc_fence_after();
@@ -1487,7 +1591,7 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint64_t* sp
             return desc0 + static_cast<uint64_t>(((blk % NS) * C::kStageBytes + off) >> 4);
         };
         for (int i = 0; i < n; ++i) {  // lo * W^T of the chunk; the very first overwrites D
-            if (FUSED && i >= kFirst) {
+            if (i >= 1) {
                 bool r = true;
                 if (lane == 0)
                     r = test_stage(g + i) || wait_stage(g + i);
@@ -1499,7 +1603,7 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint64_t* sp
             const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * pair::kPlaneBytes);
 #pragma unroll
             for (int j = 0; j < BK / 16; ++j)
-                umma_f16_pair_by(leader, d, a + a_slice<FUSED>(j, true), w + 2 * j, C::kIdesc,
+                umma_f16_pair_by(leader, d, a + fused_a_slice(j, true), w + 2 * j, C::kIdesc,
                                  (i > 0 || j > 0) ? 1u : 0u);
         }
         if (!ok)
@@ -1511,13 +1615,13 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint64_t* sp
         for (int i = 0; i < n; ++i) {  // hi * W^T; the first scales D by 2^-10 on input
             const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * pair::kPlaneBytes);
             if (i == n - 1 && g2 < total)
-                ready2 = test_chunk(g2, c2, n2);
+                ready2 = test_chunk(g2, c2);
 #pragma unroll
             for (int j = 0; j < BK / 16; ++j) {
                 if (i == 0 && j == 0)
-                    umma_f16_pair_scale10_by(leader, d, a + a_slice<FUSED>(0, false), w, C::kIdesc);
+                    umma_f16_pair_scale10_by(leader, d, a + fused_a_slice(0, false), w, C::kIdesc);
                 else
-                    umma_f16_pair_by(leader, d, a + a_slice<FUSED>(j, false), w + 2 * j, C::kIdesc, 1u);
+                    umma_f16_pair_by(leader, d, a + fused_a_slice(j, false), w + 2 * j, C::kIdesc, 1u);
             }
             umma_commit_pair_by(leader, &bars->empty[(g + i) % NS], 0x3);
         }
@@ -1527,7 +1631,7 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint64_t* sp
         kb = kb2;
         n = n2;
         if (g < total && !ready2)
-            ok = wait_chunk(g, c, n);
+            ok = wait_chunk(g, c);
     }
     if (!ok) {
         umma_commit_pair_by(leader, &bars->drain, 0x1);
@@ -1751,7 +1855,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             }
         } else if (warp == 1 && leader_cta) {
             // ---------------- MMA issuer (leader CTA) ----------------
-            pair_mma_role<BN, NS, CH, false>(bars, nullptr, smem, tmem, total, P, lane);
+            pair_mma_role<BN, NS, CH>(bars, smem, tmem, total, P, lane);
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(pair::kPromoRegs));
@@ -1783,7 +1887,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
 // values and its last 64 bytes their lo values.  A line is read whole before
 // it is written, and no line depends on another, so a thread orders only its
 // own accesses.  The MMA reads hi and lo K slices at their offsets within the
-// same 128-byte swizzled rows (a_slice<true>), in the order of the pair
+// same 128-byte swizzled rows (fused_a_slice), in the order of the pair
 // product, so both forms give identical bits.
 //
 // Signalling.  The TMA bytes of x count on a barrier of the CTA that loads
@@ -1952,7 +2056,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fpair::kThreads, 1)
             }
         } else if (warp == 1 && leader_cta) {
             // ---------------- MMA issuer (leader CTA) ----------------
-            pair_mma_role<BN, NS, CH, true>(bars, bars->sfull, smem, tmem, total, P, lane);
+            pair_mma_role_fused<BN, NS, CH>(bars, bars->sfull, smem, tmem, total, P, lane);
         }
     } else if (warp < 4 + pair::kPromoters) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(fpair::kPromoRegs));

@@ -307,6 +307,39 @@ __device__ __forceinline__ void umma_f16_pair_by(uint32_t leader, uint32_t d_tme
         : "memory");
 }
 
+// The same pair MMA with both shared-memory descriptors given as their low
+// 32-bit words (start address and leading offset) and one common high word
+// (stride offset, version, swizzle): advancing a descriptor is then a 32-bit
+// add, and the 64-bit values are put together inside the instruction's block.
+__device__ __forceinline__ void umma_pair_w_by(uint32_t leader, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                               uint32_t desc_hi, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %3};\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.ne.b32 q, %6, 0;\n\t"
+        "@q tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate), "r"(leader)
+        : "memory");
+}
+
+// D = A * B^T + D * 2^-10, descriptors as in umma_pair_w_by.
+__device__ __forceinline__ void umma_pair_w_scale10_by(uint32_t leader, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                                       uint32_t desc_hi, uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %3};\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, 1, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, p, 10;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(leader)
+        : "memory");
+}
+
 // D = A * B^T + D * 2^-10 (scale-input-d), pair form.
 __device__ __forceinline__ void umma_f16_pair_scale10_by(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
                                                          uint64_t b_desc, uint32_t idesc)
