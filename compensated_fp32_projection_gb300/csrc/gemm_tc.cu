@@ -1546,7 +1546,11 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint8_t* sme
 // (the other CTA's after a shared-memory release at cluster scope: relaxed
 // polls at cluster scope, then the acquire fence).  A chunk starts once its
 // first stage is ready, and each later stage is waited for just before its
-// first MMA, so the products of a stage overlap the split of the next.
+// first MMA, so the products of a stage overlap the split of the next.  The
+// bookkeeping is kept short as in the two-pass issuer (stages, parities and
+// 32-bit descriptor words advanced by additions); the test for the next
+// chunk stays before the last stage's hi products (testing it while the
+// first hi product waits, as the two-pass issuer does, measured slower here).
 template <int BN, int NS, int CH>
 __device__ __forceinline__ void pair_mma_role_fused(pair::Barriers* bars, uint64_t* split, uint8_t* smem,
                                                     uint32_t tmem, int total, const Problem& P, int lane)
@@ -1554,84 +1558,109 @@ __device__ __forceinline__ void pair_mma_role_fused(pair::Barriers* bars, uint64
     using C = pair::Cfg<BN, NS, CH>;
     const uint32_t leader = lane == 0 ? 1u : 0u;
     const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
-    auto test_stage = [&](int g) -> bool {
-        const int s = g % NS;
-        const uint32_t par = (g / NS) & 1;
-        if (!(mbar_test_wait(&bars->full[s], par) && mbar_test_wait_relaxed_cluster(&split[s], par)))
+    const uint32_t dlo0 = static_cast<uint32_t>(desc0);
+    const uint32_t dhi = static_cast<uint32_t>(desc0 >> 32);
+    constexpr uint32_t kSW = C::kStageBytes >> 4;
+    constexpr uint32_t kPW = pair::kPlaneBytes >> 4;
+    const int nk = P.nk;
+    auto stage_of = [](int s, uint32_t ph, int i, int& si, uint32_t& pi) {
+        si = s + i;
+        pi = ph;
+        if (si >= NS) {
+            si -= NS;
+            pi ^= 1u;
+        }
+    };
+    auto test_stage = [&](int si, uint32_t pi) -> bool {
+        if (!(mbar_test_wait(&bars->full[si], pi) && mbar_test_wait_relaxed_cluster(&split[si], pi)))
             return false;
         fence_acquire_smem_cluster();
         return true;
     };
-    auto wait_stage = [&](int g) -> bool {  // lane 0
-        const int s = g % NS;
-        const uint32_t par = (g / NS) & 1;
-        return wait_bounded(&bars->full[s], par, &bars->abort, kFaultPairMma) &&
-               wait_bounded_cluster(&split[s], par, &bars->abort, kFaultPairMma);
+    auto wait_stage = [&](int si, uint32_t pi) -> bool {  // lane 0
+        return wait_bounded(&bars->full[si], pi, &bars->abort, kFaultPairMma) &&
+               wait_bounded_cluster(&split[si], pi, &bars->abort, kFaultPairMma);
     };
-    auto test_chunk = [&](int g, int c) -> bool {
-        return (c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1)) && test_stage(g);
+    auto test_chunk = [&](int s, uint32_t ph, int c) -> bool {
+        return (c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1)) && test_stage(s, ph);
     };
-    auto wait_chunk = [&](int g, int c) -> bool {
+    auto wait_chunk = [&](int s, uint32_t ph, int c) -> bool {
         bool ok = true;
         if (lane == 0) {
-            ok = wait_stage(g);
+            ok = wait_stage(s, ph);
             if (ok && c >= 2)
                 ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort, kFaultPairMma);
         }
         return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     };
-    int g = 0, c = 0, kb = 0;
-    int n = (P.nk < CH) ? P.nk : CH;
-    bool ok = total == 0 || wait_chunk(0, 0);
+    int g = 0, c = 0, kb = 0, s = 0;
+    uint32_t ph = 0;
+    int n = nk < CH ? nk : CH;
+    bool ok = total == 0 || wait_chunk(s, ph, c);
     while (g < total && ok) {
-        const int b = c & 1;
+        const uint32_t d = tmem + (c & 1) * BN;
         tc_fence_after();
-        const uint32_t d = tmem + b * BN;
-        auto sdesc = [&](int blk, uint32_t off) {
-            return desc0 + static_cast<uint64_t>(((blk % NS) * C::kStageBytes + off) >> 4);
-        };
-        for (int i = 0; i < n; ++i) {  // lo * W^T of the chunk; the very first overwrites D
-            if (i >= 1) {
-                bool r = true;
-                if (lane == 0)
-                    r = test_stage(g + i) || wait_stage(g + i);
-                ok = __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
-                if (!ok)
-                    break;
-                tc_fence_after();
-            }
-            const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * pair::kPlaneBytes);
+        uint32_t st[CH];
+        int sidx[CH];
+        uint32_t spar[CH];
 #pragma unroll
-            for (int j = 0; j < BK / 16; ++j)
-                umma_f16_pair_by(leader, d, a + fused_a_slice(j, true), w + 2 * j, C::kIdesc,
-                                 (i > 0 || j > 0) ? 1u : 0u);
+        for (int i = 0; i < CH; ++i) {
+            stage_of(s, ph, i, sidx[i], spar[i]);
+            st[i] = dlo0 + static_cast<uint32_t>(sidx[i]) * kSW;
         }
+#pragma unroll
+        for (int i = 0; i < CH; ++i)  // lo * W^T; each later stage is waited for before its first MMA
+            if (i < n) {
+                if (i >= 1) {
+                    bool r = true;
+                    if (lane == 0)
+                        r = test_stage(sidx[i], spar[i]) || wait_stage(sidx[i], spar[i]);
+                    ok = __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)
+                    umma_pair_w_by(leader, d, st[i] + fused_a_slice(j, true), st[i] + 2 * kPW + 2 * j, dhi, C::kIdesc,
+                                   (i > 0 || j > 0) ? 1u : 0u);
+            }
         if (!ok)
             break;
         const int g2 = g + n, c2 = c + 1;
-        const int kb2 = (kb + n == P.nk) ? 0 : kb + n;
-        const int n2 = (P.nk - kb2 < CH) ? P.nk - kb2 : CH;
+        int kb2 = kb + n;
+        if (kb2 == nk)
+            kb2 = 0;
+        const int n2 = nk - kb2 < CH ? nk - kb2 : CH;
+        int s2;
+        uint32_t ph2;
+        stage_of(s, ph, n, s2, ph2);
         bool ready2 = true;
-        for (int i = 0; i < n; ++i) {  // hi * W^T; the first scales D by 2^-10 on input
-            const uint64_t a = sdesc(g + i, 0), w = sdesc(g + i, 2 * pair::kPlaneBytes);
-            if (i == n - 1 && g2 < total)
-                ready2 = test_chunk(g2, c2);
 #pragma unroll
-            for (int j = 0; j < BK / 16; ++j) {
-                if (i == 0 && j == 0)
-                    umma_f16_pair_scale10_by(leader, d, a + fused_a_slice(0, false), w, C::kIdesc);
-                else
-                    umma_f16_pair_by(leader, d, a + fused_a_slice(j, false), w + 2 * j, C::kIdesc, 1u);
+        for (int i = 0; i < CH; ++i)  // hi * W^T; the first scales D by 2^-10 on input
+            if (i < n) {
+                if (i == n - 1 && g2 < total)
+                    ready2 = test_chunk(s2, ph2, c2);
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j) {
+                    if (i == 0 && j == 0)
+                        umma_pair_w_scale10_by(leader, d, st[0] + fused_a_slice(0, false), st[0] + 2 * kPW, dhi,
+                                               C::kIdesc);
+                    else
+                        umma_pair_w_by(leader, d, st[i] + fused_a_slice(j, false), st[i] + 2 * kPW + 2 * j, dhi,
+                                       C::kIdesc, 1u);
+                }
+                umma_commit_pair_by(leader, &bars->empty[sidx[i]], 0x3);
             }
-            umma_commit_pair_by(leader, &bars->empty[(g + i) % NS], 0x3);
-        }
-        umma_commit_pair_by(leader, &bars->dfull[b], 0x3);
+        umma_commit_pair_by(leader, &bars->dfull[c & 1], 0x3);
         g = g2;
         c = c2;
         kb = kb2;
         n = n2;
+        s = s2;
+        ph = ph2;
         if (g < total && !ready2)
-            ok = wait_chunk(g, c);
+            ok = wait_chunk(s, ph, c);
     }
     if (!ok) {
         umma_commit_pair_by(leader, &bars->drain, 0x1);
