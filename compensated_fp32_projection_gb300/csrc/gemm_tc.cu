@@ -1331,7 +1331,7 @@ __global__ void __cluster_dims__(KS, 1, 1) __launch_bounds__(x2::kThreads, 1)
 // ---------------------------------------------------------------------------
 namespace pair {
 constexpr int kPromoters = 8;
-constexpr int kThreads = 128 + 32 * kPromoters;  // warpgroup 0: producer, MMA issuer, two idle warps
+constexpr int kThreads = 128 + 32 * kPromoters;  // warpgroup 0: producer, MMA issuer, its waiter, one idle warp
 // 384 threads launch with 168 registers each (pool 64512): control 40,
 // promotion 232: 128*40 + 256*232 = 64512.  The build checks the 168.
 constexpr int kLaunchRegs = 168;
@@ -1411,20 +1411,87 @@ __device__ __forceinline__ constexpr uint32_t fused_a_slice(int j, bool lo)
     return static_cast<uint32_t>((j >> 1) * (pair::kPlaneBytes >> 4) + (lo ? 4 : 0) + 2 * (j & 1));
 }
 
-// The MMA issuer of the two-pass pair product (leader CTA; the whole warp
-// runs the loop, lane 0 waits and issues), one chunk of CH K blocks at a
-// time: lo * W^T of the chunk into a fresh accumulator, then hi * W^T, whose
-// first MMA scales the accumulator by 2^-10 on input.  Stage s holds, in both
-// CTAs, the CTA's 128 rows of the hi plane (16 KB), then of the lo plane, then
-// its half of the W rows; bars->full[s] (leader) completes when both CTAs'
-// boxes have landed, and a chunk starts once all its stages are in.
-//   This thread's work between MMAs decides the pace: the tensor pipe takes
-// 112 cycles per 256 x 224 x 16 pair MMA, and issuing one takes the thread
-// 60 to 80 cycles.  So the loop keeps its bookkeeping short: the stage,
-// full-barrier parity and descriptor words of a chunk advance by additions
-// (no division), descriptors are 32-bit words, and the barrier tests for the
-// next chunk run in the window where the first hi MMA waits for the lo
-// products to finish accumulating, with the three tests issued together.
+// The chunk sequence of one CTA pair of the two-pass product: chunk c starts
+// at block g (block kb of its tile), in stage s with full-barrier parity ph,
+// and has n blocks (CH, or fewer at a tile's end).  The waiter and the MMA
+// issuer walk it in step.  Stage, parity and position advance by additions.
+template <int NS, int CH>
+struct PairChunkWalk {
+    int g = 0, c = 0, kb = 0, s = 0, n = 0;
+    uint32_t ph = 0;
+    int nk = 0;
+    __device__ __forceinline__ explicit PairChunkWalk(int nk_) : n(nk_ < CH ? nk_ : CH), nk(nk_) {}
+    __device__ __forceinline__ static void stage_of(int s0, uint32_t ph0, int i, int& si, uint32_t& pi)
+    {
+        si = s0 + i;
+        pi = ph0;
+        if (si >= NS) {
+            si -= NS;
+            pi ^= 1u;
+        }
+    }
+    __device__ __forceinline__ void next()
+    {
+        g += n;
+        ++c;
+        kb += n;
+        if (kb == nk)
+            kb = 0;
+        int s2;
+        uint32_t ph2;
+        stage_of(s, ph, n, s2, ph2);
+        s = s2;
+        ph = ph2;
+        n = nk - kb < CH ? nk - kb : CH;
+    }
+};
+
+// Waiter of the two-pass pair product (warp 2 of the leader CTA): for each
+// chunk in turn, waits until its stages have landed and its accumulator
+// buffer is back from promotion, then hands the chunk to the MMA warp through
+// a reduction at named barrier 2 + (chunk & 1) (64 threads: this warp and
+// the MMA warp).  A failed wait passes false, which ends both loops at the
+// same chunk.  The issuing thread's own mbarrier operations took hundreds of
+// cycles each while the tensor cores streamed operands through shared
+// memory; a named barrier does not go through shared memory, so the MMA warp
+// now spends its time issuing.  The waiter can be at most one chunk ahead: it
+// passes chunk c + 1 only after the MMA warp has taken chunk c, and chunk
+// c + 2 needs the accumulator that chunk c fills.
+template <int BN, int NS, int CH>
+__device__ __forceinline__ void pair_wait_role(pair::Barriers* bars, int total, const Problem& P, int lane)
+{
+    PairChunkWalk<NS, CH> w(P.nk);
+    bool ok = true;
+    while (w.g < total) {
+        if (ok && lane == 0) {
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+                if (ok && i < w.n) {
+                    int si;
+                    uint32_t pi;
+                    PairChunkWalk<NS, CH>::stage_of(w.s, w.ph, i, si, pi);
+                    ok = wait_bounded(&bars->full[si], pi, &bars->abort, kFaultPairMma);
+                }
+            if (ok && w.c >= 2)
+                ok = wait_bounded(&bars->dfree[w.c & 1], ((w.c >> 1) - 1) & 1, &bars->abort, kFaultPairMma);
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!bar_red_and(2 + (w.c & 1), 64, ok))
+            break;
+        w.next();
+    }
+}
+
+// The MMA issuer of the two-pass pair product (leader CTA, warp 1; the whole
+// warp runs the loop, lane 0 issues), one chunk of CH K blocks at a time,
+// each handed over by the waiter warp: lo * W^T of the chunk into a fresh
+// accumulator, then hi * W^T, whose first MMA scales the accumulator by
+// 2^-10 on input.  Stage s holds, in both CTAs, the CTA's 128 rows of the hi
+// plane (16 KB), then of the lo plane, then its half of the W rows.  The
+// tensor pipe takes 112 cycles per 256 x 224 x 16 pair MMA and issuing one
+// takes this thread 60 to 70, so the loop does nothing else between MMAs:
+// descriptors are 32-bit words advanced by additions, and the commits that
+// give the stages and the accumulator back are its only mbarrier accesses.
 template <int BN, int NS, int CH>
 __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint8_t* smem, uint32_t tmem, int total,
                                               const Problem& P, int lane)
@@ -1434,63 +1501,25 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint8_t* sme
     const uint64_t desc0 = sw128_kmajor_desc(smem_u32(smem));
     const uint32_t dlo0 = static_cast<uint32_t>(desc0);
     const uint32_t dhi = static_cast<uint32_t>(desc0 >> 32);
-    constexpr uint32_t kSW = C::kStageBytes >> 4;     // one stage, in descriptor units
-    constexpr uint32_t kPW = pair::kPlaneBytes >> 4;  // one plane box
-    const int nk = P.nk;
-    // stage and full-barrier parity of block i of a chunk whose first block
-    // sits at stage s with parity ph (CH <= NS: the ring wraps at most once)
-    auto stage_of = [](int s, uint32_t ph, int i, int& si, uint32_t& pi) {
-        si = s + i;
-        pi = ph;
-        if (si >= NS) {
-            si -= NS;
-            pi ^= 1u;
-        }
-    };
-    auto test_chunk = [&](int s, uint32_t ph, int c, int n) -> bool {
-        uint32_t r = (c < 2 || mbar_test_wait(&bars->dfree[c & 1], ((c >> 1) - 1) & 1)) ? 1u : 0u;
-#pragma unroll
-        for (int i = 0; i < CH; ++i)
-            if (i < n) {
-                int si;
-                uint32_t pi;
-                stage_of(s, ph, i, si, pi);
-                r &= mbar_test_wait(&bars->full[si], pi) ? 1u : 0u;
-            }
-        return r != 0;
-    };
-    auto wait_chunk = [&](int s, uint32_t ph, int c, int n) -> bool {
-        bool ok = true;
-        if (lane == 0) {
-#pragma unroll
-            for (int i = 0; i < CH; ++i)
-                if (ok && i < n) {
-                    int si;
-                    uint32_t pi;
-                    stage_of(s, ph, i, si, pi);
-                    ok = wait_bounded(&bars->full[si], pi, &bars->abort, kFaultPairMma);
-                }
-            if (ok && c >= 2)
-                ok = wait_bounded(&bars->dfree[c & 1], ((c >> 1) - 1) & 1, &bars->abort, kFaultPairMma);
-        }
-        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    };
-    // chunk c starts at block g (block kb of its tile), stage s, parity ph, and has n blocks
-    int g = 0, c = 0, kb = 0, s = 0;
-    uint32_t ph = 0;
-    int n = nk < CH ? nk : CH;
-    bool ok = total == 0 || wait_chunk(s, ph, c, n);
-    while (g < total && ok) {
-        const uint32_t d = tmem + (c & 1) * BN;
+    constexpr uint32_t kSW = C::kStageBytes >> 4;
+    constexpr uint32_t kPW = pair::kPlaneBytes >> 4;
+    PairChunkWalk<NS, CH> w(P.nk);
+    bool ok = true;
+    while (w.g < total) {
+        ok = bar_red_and(2 + (w.c & 1), 64, true);
+        if (!ok)
+            break;
+        const uint32_t d = tmem + (w.c & 1) * BN;
         tc_fence_after();
-        uint32_t st[CH];  // descriptor word of each stage of the chunk
+        uint32_t st[CH];
         int sidx[CH];
 #pragma unroll
         for (int i = 0; i < CH; ++i) {
             uint32_t pi;
-            stage_of(s, ph, i, sidx[i], pi);
+            PairChunkWalk<NS, CH>::stage_of(w.s, w.ph, i, sidx[i], pi);
             st[i] = dlo0 + static_cast<uint32_t>(sidx[i]) * kSW;
         }
+        const int n = w.n;
 #pragma unroll
         for (int i = 0; i < CH; ++i)  // lo * W^T of the chunk; the very first overwrites D
             if (i < n) {
@@ -1499,16 +1528,6 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint8_t* sme
                     umma_pair_w_by(leader, d, st[i] + kPW + 2 * j, st[i] + 2 * kPW + 2 * j, dhi, C::kIdesc,
                                    (i > 0 || j > 0) ? 1u : 0u);
             }
-        // the next chunk, and whether its stages and accumulator are ready
-        const int g2 = g + n, c2 = c + 1;
-        int kb2 = kb + n;
-        if (kb2 == nk)
-            kb2 = 0;
-        const int n2 = nk - kb2 < CH ? nk - kb2 : CH;
-        int s2;
-        uint32_t ph2;
-        stage_of(s, ph, n, s2, ph2);
-        const bool ready2 = g2 >= total || test_chunk(s2, ph2, c2, n2);
 #pragma unroll
         for (int i = 0; i < CH; ++i)  // hi * W^T; the first scales D by 2^-10 on input
             if (i < n) {
@@ -1521,15 +1540,8 @@ __device__ __forceinline__ void pair_mma_role(pair::Barriers* bars, uint8_t* sme
                 }
                 umma_commit_pair_by(leader, &bars->empty[sidx[i]], 0x3);
             }
-        umma_commit_pair_by(leader, &bars->dfull[c & 1], 0x3);
-        g = g2;
-        c = c2;
-        kb = kb2;
-        n = n2;
-        s = s2;
-        ph = ph2;
-        if (g < total && !ready2)
-            ok = wait_chunk(s, ph, c, n);
+        umma_commit_pair_by(leader, &bars->dfull[w.c & 1], 0x3);
+        w.next();
     }
     if (!ok) {
         umma_commit_pair_by(leader, &bars->drain, 0x1);
@@ -1885,6 +1897,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         } else if (warp == 1 && leader_cta) {
             // ---------------- MMA issuer (leader CTA) ----------------
             pair_mma_role<BN, NS, CH>(bars, smem, tmem, total, P, lane);
+        } else if (warp == 2 && leader_cta) {
+            // ---------------- waiter for the MMA issuer (leader CTA) ----------------
+            pair_wait_role<BN, NS, CH>(bars, total, P, lane);
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(pair::kPromoRegs));

@@ -340,6 +340,22 @@ __device__ __forceinline__ void umma_pair_w_scale10_by(uint32_t leader, uint32_t
         : "memory");
 }
 
+// Named-barrier reduction: blocks until `count` threads of the CTA have
+// arrived at barrier `id`, and returns the AND of their predicates.
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t count, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %2, 0;\n\t"
+        "bar.red.and.pred p, %1, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(v ? 1u : 0u), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // D = A * B^T + D * 2^-10 (scale-input-d), pair form.
 __device__ __forceinline__ void umma_f16_pair_scale10_by(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
                                                          uint64_t b_desc, uint32_t idesc)
