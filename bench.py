@@ -50,6 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 LEGS = ("step", "split", "product", "fused", "ws", "merge", "simt", "geglu")
+BREAKDOWN_STEPS = 200  # steps of the second loop that times the split and the product of a step apart
 
 
 def parse():
@@ -461,6 +462,24 @@ def run_ours(args):
     for _ in range(args.steps):
         flush()
         a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        events.append((a, b))
+    barrier()
+    clocks = sampler.stop()
+    times = [a.elapsed_time(b) for a, b in events]  # ms, whole step
+    ms = max_over_ranks(statistics.mean(times), dist, dev)
+    # the split and the product of a step, timed separately in a second loop:
+    # an event between the two launches keeps the product from being launched
+    # while the split still runs (its set-up then no longer overlaps the
+    # split), so the steps of this loop are slower than the timed ones and the
+    # product's time here includes its set-up
+    breakdown = []
+    for _ in range(min(args.steps, BREAKDOWN_STEPS)):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
         m = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -468,13 +487,11 @@ def run_ours(args):
         m.record(stream)
         product()
         b.record(stream)
-        events.append((a, m, b))
+        breakdown.append((a, m, b))
     barrier()
-    clocks = sampler.stop()
-    times = [a.elapsed_time(b) for a, _, b in events]  # ms, whole step
-    split_times = [a.elapsed_time(m) for a, m, _ in events]
-    product_times = [m.elapsed_time(b) for _, m, b in events]
-    ms = max_over_ranks(statistics.mean(times), dist, dev)
+    split_times = [a.elapsed_time(m) for a, m, _ in breakdown]
+    product_times = [m.elapsed_time(b) for _, m, b in breakdown]
+    breakdown_step_ms = statistics.mean(a.elapsed_time(b) for a, _, b in breakdown)
     st, where = pkg.device_status()
     if st != 0:
         raise RuntimeError(f"kernel fault word {where:#x}")
@@ -684,6 +701,9 @@ def run_ours(args):
             "traffic": traffic,
             "peak_source": f"{peak_src} dense bf16 burst (FP16 runs at the same tensor rate)",
             "work": "4*M*N*K tensor FLOP per launch (hi and lo products)",
+            "kernel_time": f"mean of {len(product_times)} product launches, each timed between an event after the "
+                           f"step's split and one after the product (a second loop of steps; with the event between "
+                           f"them a step took {breakdown_step_ms:.4f} ms against {ms:.4f} without)",
             "step_frac_of_roofline": value / world / (peaks["bf16_tflops"] / 2.0),
         },
         "e2e": {
