@@ -294,23 +294,11 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 
 // D (both CTAs' tensor memory, M = 256) = A * B^T (+ D), A and B from both
 // CTAs' shared memory at the descriptors' offsets; issued by one lane of the
-// pair's leader CTA (`leader` nonzero).
-__device__ __forceinline__ void umma_f16_pair_by(uint32_t leader, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "setp.ne.b32 q, %5, 0;\n\t"
-        "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
-        : "memory");
-}
-
-// The same pair MMA with both shared-memory descriptors given as their low
-// 32-bit words (start address and leading offset) and one common high word
-// (stride offset, version, swizzle): advancing a descriptor is then a 32-bit
-// add, and the 64-bit values are put together inside the instruction's block.
+// pair's leader CTA (`leader` nonzero).  Both shared-memory descriptors are
+// given as their low 32-bit words (start address and leading offset) and one
+// common high word (stride offset, version, swizzle): advancing a descriptor
+// is then a 32-bit add, and the 64-bit values are put together inside the
+// instruction's block.
 __device__ __forceinline__ void umma_pair_w_by(uint32_t leader, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                                uint32_t desc_hi, uint32_t idesc, uint32_t accumulate)
 {
@@ -354,19 +342,6 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t count, bool v)
         : "r"(id), "r"(v ? 1u : 0u), "r"(count)
         : "memory");
     return r != 0;
-}
-
-// D = A * B^T + D * 2^-10 (scale-input-d), pair form.
-__device__ __forceinline__ void umma_f16_pair_scale10_by(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
-                                                         uint64_t b_desc, uint32_t idesc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.b32 p, 1, 0;\n\t"
-        "setp.ne.b32 q, %4, 0;\n\t"
-        "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p, 10;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(leader)
-        : "memory");
 }
 
 // Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
