@@ -1454,9 +1454,11 @@ struct PairChunkWalk {
 // same chunk.  The issuing thread's own mbarrier operations took hundreds of
 // cycles each while the tensor cores streamed operands through shared
 // memory; a named barrier does not go through shared memory, so the MMA warp
-// now spends its time issuing.  The waiter can be at most one chunk ahead: it
-// passes chunk c + 1 only after the MMA warp has taken chunk c, and chunk
-// c + 2 needs the accumulator that chunk c fills.
+// now spends its time issuing.  A hand-off completes only when both warps
+// have arrived, so neither can be more than one hand-off ahead of the other.
+// Ordering: the waiter observes the stages' and the accumulator's barriers,
+// the named barrier orders that before the MMA warp's
+// tcgen05.fence::after_thread_sync, and the MMAs follow the fence.
 template <int BN, int NS, int CH>
 __device__ __forceinline__ void pair_wait_role(pair::Barriers* bars, int total, const Problem& P, int lane)
 {
