@@ -124,15 +124,18 @@ comp_status_t gemm_ws_impl(const float* x, const uint16_t* W, float* y, int64_t 
         (overlap(workspace, workspace_bytes, x, 4 * M * K) || overlap(workspace, workspace_bytes, W, 2 * N * K) ||
          overlap(workspace, workspace_bytes, y, 4 * M * N)))
         return COMP_ERR_INVALID_VALUE;
-    // at most 32 rows against a wide W: one kernel with the split fused needs
-    // no workspace and is faster than the two-pass form
-    if (swap_fused_preferred(x, W, M, N, K))
-        return launch_swap_fused(x, W, y, M, N, K, dev, s, epi);
     uint16_t* const ws = static_cast<uint16_t*>(workspace);
     const bool ws_aligned = (reinterpret_cast<uintptr_t>(workspace) & 15u) == 0;
-    // two-pass form on the caller's W: planes [M, K] in the workspace
     const int64_t need = comp_gemm_workspace_bytes(M, K);
-    if (ws && ws_aligned && need > 0 && workspace_bytes >= need && gemm_f16x2_supported(ws, ws + M * K, W, K)) {
+    const bool planes_fit =
+        ws && ws_aligned && need > 0 && workspace_bytes >= need && gemm_f16x2_supported(ws, ws + M * K, W, K);
+    // at most 32 rows against a wide W: one kernel with the split fused needs
+    // no workspace and is faster than the two-pass form, except with 17 to 32
+    // rows or few W tiles and a long K, where the two-pass form is faster
+    if (swap_fused_preferred(x, W, M, N, K) && !(planes_fit && swap_two_pass_better(M, N, K)))
+        return launch_swap_fused(x, W, y, M, N, K, dev, s, epi);
+    // two-pass form on the caller's W: planes [M, K] in the workspace
+    if (planes_fit) {
         const comp_status_t sp = launch_split(x, ws, ws + M * K, M * K, dev, s);
         if (sp != COMP_OK)
             return sp;

@@ -2922,9 +2922,11 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     P.stall = stall ? 1 : 0;
     CUtensorMap th{}, tl{}, tw{};
     // at most 32 rows and at least 32 tiles of 128 columns: operands swapped,
-    // W streams through full 128-row MMAs
+    // W streams through full 128-row MMAs (one CTA per tile, each streaming
+    // about 40-50 GB/s of W); with few tiles and a long K the split-K path
+    // below puts more CTAs on W
     const int64_t t128 = (N + swp::kTileN - 1) / swp::kTileN;
-    if (variant == 3 || (variant == 0 && M <= 32 && t128 >= 32)) {
+    if (variant == 3 || (variant == 0 && M <= 32 && t128 >= 32 && !swap_few_tiles_long_k(N, K))) {
         const uint32_t mp = M <= 16 ? 16u : 32u;
         P.tiles_m = 1;
         P.tiles_n = static_cast<int>(t128);
@@ -3019,6 +3021,25 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     if (bn == 128)
         return launch_x2_bn<128, 4, 2>(th, tl, tw, P, dev, stream);
     return launch_x2_bn<96, 4, 2>(th, tl, tw, P, dev, stream);
+}
+
+bool swap_few_tiles_long_k(int64_t N, int64_t K)
+{
+    // measured on GB300 (cold, L2 flushed): 16 x 4096 x 14336 took 69.6 us
+    // swapped against 53.3 us with K split over clusters of 4; at
+    // 16 x 4096 x 4096 the swapped kernel wins (24.6 against 30.7 us)
+    return (N + swp::kTileN - 1) / swp::kTileN <= 40 && (K + BK - 1) / BK >= 96;
+}
+
+bool swap_two_pass_better(int64_t M, int64_t N, int64_t K)
+{
+    // given a workspace: with 17 to 32 rows the fused kernel holds three
+    // 64 KB stages against the two-pass swapped product's four (32 x 4096 x
+    // 4096: 36.9 us fused, 26.6 us product + 6.1 us split, cold); with few
+    // tiles and a long K the two-pass form splits K (above).  A short K stays
+    // on the one-launch kernel.
+    const bool short_k = (K + BK - 1) / BK <= 8;
+    return !short_k && (M > 16 || swap_few_tiles_long_k(N, K));
 }
 
 bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K)

@@ -224,7 +224,10 @@ int64_t comp_gemm_workspace_bytes_mnk(int64_t M, int64_t N, int64_t K);
  *   - M <= 32 against at least 32 * 128 rows of W or with K <= 512, K a
  *     multiple of 8, x and W 16-byte aligned: the fused swapped-operand kernel
  *     of comp_gemm_f32x16 instead (one launch; faster there than split plus
- *     product); the workspace is unused.
+ *     product); the workspace is unused.  Except, when the planes fit the
+ *     workspace and K > 512: with 17 to 32 rows, or with W of at most
+ *     40 * 128 rows and K >= 6081 (96 blocks of 64), the two-pass form below
+ *     is faster and runs instead.
  *   - K a multiple of 8, W 16-byte aligned, workspace of at least
  *     comp_gemm_workspace_bytes(M, K): the planes [M, K] (hi, then lo) and
  *     the caller's W.

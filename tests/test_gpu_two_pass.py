@@ -346,3 +346,25 @@ def test_product_bit_exact_through_identity(pkg, orc, variant, M):
     y = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), variant).cpu().numpy()
     y_or = orc.gemm_comp(x.numpy(), W.view(torch.int16).numpy().view(np.uint16))
     assert np.array_equal(y.view(np.uint32), y_or.view(np.uint32)), int(np.sum(y.view(np.uint32) != y_or.view(np.uint32)))
+
+
+# At most 32 rows, given a workspace: 17 to 32 rows against a wide W, or few
+# tiles of W with a long K, run the two-pass form (split, then the swapped
+# product or K split over clusters) instead of the one-launch swapped kernel;
+# the result is the explicit split + product's, bit for bit, and the oracle's
+# within the gate.
+@pytest.mark.parametrize("shape", [(32, 4096, 4096), (24, 4100, 1032), (16, 4096, 14336), (8, 3000, 6208)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_ws_routes_decode_shapes_to_the_two_pass_form(pkg, orc, shape):
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=M + N + K, scale=2.0)
+    xd, Wd = x.cuda(), W.cuda()
+    y = pkg.comp_gemm_f32x16_ws(xd, Wd)
+    hi, lo = pkg.comp_split_f32(xd)
+    y2 = pkg.comp_gemm_f16x2(hi, lo, Wd)
+    assert torch.equal(bits(y), bits(y2))
+    r, c = sample_outputs(M, N)
+    e_gpu, e_cast = check_comp(y, x, W, orc, r, c)
+    assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
