@@ -625,9 +625,12 @@ def run_ours(args):
         swapped = so.M <= 32 and (so.N + 127) // 128 >= 32 and not padded
         swapped = swapped or (so.M <= 32 and (so.K + 63) // 64 <= 8 and not padded)
         t128 = ((so.M + 127) // 128) * ((so.N + 127) // 128)
-        nk = (so.K + 7) // 8 * 8 // 64
-        splitk = so.M > 32 and (so.M <= 128 or so.M * so.N < 152 * 128 * 192) and (
-            (t128 * 4 <= 152 and nk >= 16) or (t128 * 2 <= 152 and nk >= 8))
+        t64 = ((so.M + 127) // 128) * ((so.N + 63) // 64)
+        nk = ((so.K + 7) // 8 * 8 + 63) // 64
+        few = so.M > 32 and (so.M <= 128 or so.M * so.N < 152 * 128 * 192)  # not the CTA-pair kernel
+        narrow = few and t128 * 2 <= 152 and nk <= 32 and ((t64 * 2 <= 152 and nk >= 8) or t64 <= 152)
+        narrow_split = narrow and t64 * 2 <= 152 and nk >= 8
+        splitk = few and not narrow and ((t128 * 4 <= 152 and nk >= 16) or (t128 * 2 <= 152 and nk >= 8))
         if swapped:
             path = "one kernel: operands swapped (y^T = W x^T), split fused"
         elif padded:
@@ -635,7 +638,11 @@ def run_ours(args):
                    "kernel" % ((so.K + 7) // 8 * 8)
         else:
             path = "split + product kernel"
-        if splitk:
+        if narrow_split:
+            path += ", 128 x 64 tiles, K split over pairs of CTAs (ordered reduction through distributed shared memory)"
+        elif narrow:
+            path += ", 128 x 64 tiles, one CTA each"
+        elif splitk:
             path += ", K split over clusters of CTAs (ordered reduction through distributed shared memory)"
         others[name] = {
             "M": so.M, "N": so.N, "K": so.K,

@@ -2976,9 +2976,10 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
                          : launch_pair_bn<256, 4, 2>(th, tl, tw, ty, P, dev, stream);
     }
     // few tiles: split K over clusters of 2 or 4 CTAs (at most 32 rows:
-    // 192-wide tiles reduced in the leader; otherwise 128 x 128 tiles reduced
-    // across the cluster)
+    // 192-wide tiles reduced in the leader; otherwise 128 x 128 tiles, or
+    // 128 x 64 tiles with a short K, reduced across the cluster)
     int ks = 1;
+    bool narrow = false;  // 128 x 64 tiles
     if (M <= 32) {
         const int64_t t192 = (N + 191) / 192;
         if (t192 * 4 <= dev.sm_count && P.nk >= 16)
@@ -2987,12 +2988,31 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
             ks = 2;
     } else {
         const int64_t t128 = ((M + BM - 1) / BM) * ((N + 127) / 128);
-        if (t128 * 4 <= dev.sm_count && P.nk >= 16)
-            ks = 4;
-        else if (t128 * 2 <= dev.sm_count && P.nk >= 8)
-            ks = 2;
+        const int64_t t64 = ((M + BM - 1) / BM) * ((N + 63) / 64);
+        if (t128 * 2 <= dev.sm_count && P.nk <= 32) {
+            // few tiles and K at most 2048: twice as many 64-wide tiles, with K
+            // split over pairs if they fit one wave, else unsplit.  Each rank
+            // then has half the partial sums to send, or none (GB300, product
+            // from the planes, cold / back to back: 512 x 1024 x 1024 16.4 /
+            // 12.3 us against 18.4 / 13.8 for 128-wide tiles split over 4;
+            // 1000 x 776 x 1032 unsplit 20.5 / 15.1 against 22.5 / 17.3 split
+            // over 2).  With a longer K the narrow MMAs lose (512 x 512 x 4096:
+            // 30.7 against 28.7 us).
+            if (t64 * 2 <= dev.sm_count && P.nk >= 8) {
+                ks = 2;
+                narrow = true;
+            } else if (t64 <= dev.sm_count) {
+                narrow = true;
+            }
+        }
+        if (!narrow) {
+            if (t128 * 4 <= dev.sm_count && P.nk >= 16)
+                ks = 4;
+            else if (t128 * 2 <= dev.sm_count && P.nk >= 8)
+                ks = 2;
+        }
     }
-    const int bn = ks > 1 ? (M <= 32 ? 192 : 128) : pick_bn_x2(M, N, dev.sm_count);
+    const int bn = narrow ? 64 : ks > 1 ? (M <= 32 ? 192 : 128) : pick_bn_x2(M, N, dev.sm_count);
     P.tiles_m = static_cast<int>((M + BM - 1) / BM);
     P.tiles_n = static_cast<int>((N + bn - 1) / bn);
     if (static_cast<int64_t>(P.tiles_m) * P.tiles_n * P.nk > INT32_MAX / 2)
@@ -3003,6 +3023,9 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
         !encode_2d(&tl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, lo, K, M, BK, box_rows) ||
         !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, W, K, N, BK, static_cast<uint32_t>(bn)))
         return COMP_ERR_CUDA;
+    if (narrow)
+        return ks == 2 ? launch_x2_splitk<64, 4, 2, BM, 2>(th, tl, tw, P, dev, stream)
+                       : launch_x2_bn<64, 4, 2>(th, tl, tw, P, dev, stream);
     if (ks == 4)
         return M <= 32 ? launch_x2_splitk<192, 6, 2, 32, 4>(th, tl, tw, P, dev, stream)
                        : launch_x2_splitk<128, 3, 2, BM, 4>(th, tl, tw, P, dev, stream);
