@@ -622,8 +622,7 @@ def run_ours(args):
         byts = 4 * so.M * so.K + 2 * so.N * so.K + 4 * so.M * so.N
         t_star = max(4.0 * so.M * so.N * so.K / (peaks_now["bf16_tflops"] * 1e12), byts / (peaks_now["hbm_gbs"] * 1e9))
         padded = so.K % 8 != 0
-        swapped = so.M <= 32 and (so.N + 127) // 128 >= 32 and not padded
-        swapped = swapped or (so.M <= 32 and (so.K + 63) // 64 <= 8 and not padded)
+        swapped = so.M <= 32 and not padded
         t128 = ((so.M + 127) // 128) * ((so.N + 127) // 128)
         t64 = ((so.M + 127) // 128) * ((so.N + 63) // 64)
         nk = ((so.K + 7) // 8 * 8 + 63) // 64
@@ -632,7 +631,12 @@ def run_ours(args):
         narrow_split = narrow and t64 * 2 <= 152 and nk >= 8
         splitk = few and not narrow and ((t128 * 4 <= 152 and nk >= 16) or (t128 * 2 <= 152 and nk >= 8))
         if swapped:
+            tiles_w = (so.N + 127) // 128
+            nk_w = (so.K + 63) // 64
+            ks_w = 4 if tiles_w * 4 <= 152 and nk_w >= 16 else 2 if tiles_w * 2 <= 152 and nk_w >= 8 else 1
             path = "one kernel: operands swapped (y^T = W x^T), split fused"
+            if ks_w > 1:
+                path += ", K split over clusters of %d CTAs" % ks_w
         elif padded:
             path = "one prep launch (x split into planes and W copied, both padded to K = %d), then the product " \
                    "kernel" % ((so.K + 7) // 8 * 8)

@@ -129,10 +129,10 @@ comp_status_t gemm_ws_impl(const float* x, const uint16_t* W, float* y, int64_t 
     const int64_t need = comp_gemm_workspace_bytes(M, K);
     const bool planes_fit =
         ws && ws_aligned && need > 0 && workspace_bytes >= need && gemm_f16x2_supported(ws, ws + M * K, W, K);
-    // at most 32 rows against a wide W: one kernel with the split fused needs
-    // no workspace and is faster than the two-pass form, except with 17 to 32
-    // rows or few W tiles and a long K, where the two-pass form is faster
-    if (swap_fused_preferred(x, W, M, N, K) && !(planes_fit && swap_two_pass_better(M, N, K)))
+    // at most 32 rows: one kernel with the split fused needs no workspace and
+    // is as fast as the two-pass form or faster, except with 17 to 32 rows and
+    // no split of K
+    if (swap_fused_preferred(x, W, M, N, K) && !(planes_fit && swap_two_pass_better(M, N, K, dev.sm_count)))
         return launch_swap_fused(x, W, y, M, N, K, dev, s, epi);
     // two-pass form on the caller's W: planes [M, K] in the workspace
     if (planes_fit) {

@@ -1006,8 +1006,9 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
         for (int g0 = 0, tt = 0; g0 < total; g0 += nkr, ++tt, t += groups) {
             if (warp == 4)
                 (void)lane0_wait(&bars->dfull[0], tt & 1, &bars->abort, kFaultX2Promote);
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * x2::kPromoters) : "memory");
-            if (*reinterpret_cast<volatile int*>(&bars->abort))
+            // one verdict for all promotion warps: a flag read by each warp after a
+            // plain barrier could change between their reads
+            if (bar_red_or(1, 32 * x2::kPromoters, *reinterpret_cast<volatile int*>(&bars->abort) != 0))
                 break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + wh * C::kHalf;
@@ -1219,8 +1220,9 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
             // (no shared-memory traffic) and read the verdict from the abort flag
             if (warp == 4)
                 (void)lane0_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultX2Promote);
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * x2::kPromoters) : "memory");
-            if (*reinterpret_cast<volatile int*>(&bars->abort))
+            // one verdict for all promotion warps: a flag read by each warp after a
+            // plain barrier could change between their reads
+            if (bar_red_or(1, 32 * x2::kPromoters, *reinterpret_cast<volatile int*>(&bars->abort) != 0))
                 break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * BN + wh * C::kHalf;
@@ -1712,8 +1714,9 @@ __device__ __forceinline__ void pair_promote_role(pair::Barriers* bars, const CU
         // one warp polls the barrier; the others wait at a named barrier
         if (warp == 4)
             (void)lane0_wait(&bars->dfull[b], (c >> 1) & 1, &bars->abort, kFaultPairPromote);
-        asm volatile("bar.sync 1, %0;" ::"n"(32 * pair::kPromoters) : "memory");
-        if (*reinterpret_cast<volatile int*>(&bars->abort))
+        // one verdict for all promotion warps: a flag read by each warp after a
+        // plain barrier could change between their reads
+        if (bar_red_or(1, 32 * pair::kPromoters, *reinterpret_cast<volatile int*>(&bars->abort) != 0))
             break;
         tc_fence_after();
         const uint32_t taddr = tmem + (static_cast<uint32_t>(wq * 32) << 16) + b * BN + wh * C::kHalf;
@@ -2176,17 +2179,21 @@ constexpr int kThreads = 128 + 32 * kPromoters;  // warpgroup 0: producer, MMA i
 constexpr int kTileN = 128;                       // W rows per tile (the MMA's M)
 constexpr int kMaxStages = 8;
 
-template <int MP, int BPS, int NS, bool FX>
+template <int MP, int BPS, int NS, bool FX, int KS = 1>
 struct Cfg {
     static_assert(MP == 16 || MP == 32, "padded rows of x");
     static_assert(BPS >= 1 && BPS <= 8 && NS >= 2 && NS <= kMaxStages, "pipeline");
+    static_assert(KS == 1 || KS == 2 || KS == 4, "split K over a cluster of 1, 2 or 4 CTAs");
     static constexpr uint32_t kWBox = kTileN * BK * 2;  // 16 KB: one K block of the W tile
     static constexpr uint32_t kXBox = MP * BK * 2;      // one plane's Mp rows of one K block
     static constexpr uint32_t kXF = MP * BK * 4;        // FX: the FP32 x rows of one K block
     static constexpr uint32_t kXFOff = BPS * (kWBox + 2 * kXBox);
     static constexpr uint32_t kStageBytes = kXFOff + (FX ? BPS * kXF : 0u);
     static_assert(kXBox % 1024 == 0, "128-byte swizzle atoms");
-    static constexpr size_t kSmem = 1024 + NS * kStageBytes + 512;
+    // split K: the partial sums of the columns this rank owns, one slot per
+    // rank of the cluster: (4 / KS) warps x 32 lanes x (Mp hi, then Mp lo)
+    static constexpr uint32_t kRedBytes = KS > 1 ? static_cast<uint32_t>(KS * (4 / KS) * 32 * 2 * MP * 4) : 0u;
+    static constexpr size_t kSmem = 1024 + NS * kStageBytes + 512 + kRedBytes;
     static_assert(kSmem <= 232448, "shared memory");
     static constexpr int kCols = 2 * MP;               // accumulator columns per buffer
     static constexpr uint32_t kTmemCols = 2 * kCols;  // two buffers (64 or 128 columns)
@@ -2200,6 +2207,8 @@ struct Barriers {
     uint64_t dfull[2];
     uint64_t dfree[2];
     uint64_t drain;
+    uint64_t rs_full[4];  // split K, owner: the other ranks' partial sums of warp w's columns landed
+    uint64_t rs_done[4];  // split K, other ranks: the owner has read warp w's slot of the previous tile
     uint32_t tmem_base;
     int abort;
 };
@@ -2210,14 +2219,47 @@ constexpr uint32_t kFaultSwpProducer = 0x801;
 constexpr uint32_t kFaultSwpMma = 0x802;
 constexpr uint32_t kFaultSwpPromote = 0x803;
 constexpr uint32_t kFaultSwpSplit = 0x804;
+constexpr uint32_t kFaultSwpReduce = 0x805;
+
+// Bounded wait, by lane 0 of a warp, for a barrier that other CTAs of the
+// cluster arrive on with release at cluster scope; then every lane takes the
+// phase with acquire at cluster scope itself, so that each may read what the
+// arrivals published.
+__device__ __forceinline__ bool warp_wait_acquire_cluster(uint64_t* bar, uint32_t parity, int* abort_flag,
+                                                          uint32_t code)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) {
+        const long long start = clock64();
+        while (!mbar_try_wait_acquire_cluster(bar, parity)) {
+            if (*reinterpret_cast<volatile int*>(abort_flag) || clock64() - start > kWaitLimit) {
+                atomicCAS(&g_fault_word, 0u, code);
+                *reinterpret_cast<volatile int*>(abort_flag) = 1;
+                ok = false;
+                break;
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (ok)
+        (void)mbar_try_wait_acquire_cluster(bar, parity);
+    return ok;
+}
 
 // FX: tmap_hi is the map of FP32 x (boxes of 64 x Mp, no swizzle); tmap_lo is unused.
-template <int MP, int BPS, int NS, bool FX, bool EPI>
-__global__ void __launch_bounds__(swp::kThreads, 1)
-    comp_f16x2_swap_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
-                           const __grid_constant__ CUtensorMap tmap_w, const Problem P)
+// KS > 1: a cluster of KS CTAs per tile, rank r taking the r-th of KS
+// contiguous ranges of the K blocks; at the tile end rank r owns the tile's
+// columns 128 r / KS .. 128 (r + 1) / KS - 1: the other ranks' promotion warps
+// store their partial hi and lo sums of those columns into its receive buffer
+// (distributed shared memory) and arrive on its barrier with release at
+// cluster scope; the owner adds the KS partial sums in rank order (binary32,
+// round to nearest even), so reruns give identical bits, then merges and
+// stores y, and gives each slot back.
+template <int MP, int BPS, int NS, bool FX, bool EPI, int KS>
+__device__ __forceinline__ void swap_kernel_body(const CUtensorMap& tmap_hi, const CUtensorMap& tmap_lo,
+                                                 const CUtensorMap& tmap_w, const Problem& P)
 {
-    using C = swp::Cfg<MP, BPS, NS, FX>;
+    using C = swp::Cfg<MP, BPS, NS, FX, KS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     swp::Barriers* bars = reinterpret_cast<swp::Barriers*>(smem + NS * C::kStageBytes);
@@ -2225,10 +2267,16 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    const int rank = KS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int cid = static_cast<int>(blockIdx.x) / KS;  // the cluster (one tile at a time)
+    const int ncl = static_cast<int>(gridDim.x) / KS;
     const int num_tiles = P.tiles_n;  // tiles of 128 columns of y (rows of W)
-    const int my_tiles =
-        static_cast<int>(blockIdx.x) < num_tiles ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
-    const int spt = (P.nk + BPS - 1) / BPS;  // stages per tile; the last may hold fewer blocks
+    const int my_tiles = cid < num_tiles ? (num_tiles - 1 - cid) / ncl + 1 : 0;
+    // this rank's K blocks of every tile: [kb_lo, kb_hi), at least one (the host
+    // splits K only when every rank gets some)
+    const int kb_lo = static_cast<int>(static_cast<int64_t>(P.nk) * rank / KS);
+    const int kb_hi = static_cast<int>(static_cast<int64_t>(P.nk) * (rank + 1) / KS);
+    const int spt = (kb_hi - kb_lo + BPS - 1) / BPS;  // stages per tile; the last may hold fewer blocks
     const int total = my_tiles * spt;
 
     if (threadIdx.x == 0) {
@@ -2242,6 +2290,10 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             mbar_init(&bars->dfree[b], swp::kPromoters);
         }
         mbar_init(&bars->drain, 1);
+        for (int w = 0; w < 4; ++w) {
+            mbar_init(&bars->rs_full[w], KS > 1 ? KS - 1 : 1);
+            mbar_init(&bars->rs_done[w], 1);
+        }
         bars->abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -2256,6 +2308,8 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (KS > 1)
+        cluster_sync();  // every rank's barriers initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
@@ -2263,13 +2317,13 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
         // ---------------- TMA producer: per stage, BPS K blocks of the W tile and of both planes ----------------
         int issued = 0;
         grid_dependency_wait();  // the planes come from the previous kernel of the stream
-        int t = static_cast<int>(blockIdx.x), sk = 0;
+        int t = cid, sk = 0;
         for (int g = 0; g < total; ++g) {
             const int s = g % NS;
             if (g >= NS && !wait_bounded(&bars->empty[s], ((g / NS) - 1) & 1, &bars->abort, kFaultSwpProducer))
                 break;
-            const int kb0 = sk * BPS;
-            const int n = P.nk - kb0 < BPS ? P.nk - kb0 : BPS;
+            const int kb0 = kb_lo + sk * BPS;
+            const int n = kb_hi - kb0 < BPS ? kb_hi - kb0 : BPS;
             uint8_t* st = smem + s * C::kStageBytes;
             if (FX) {  // the FP32 x rows first: the split warps need them before the MMA needs W
                 mbar_arrive_expect_tx(&bars->xfull[s], n * C::kXF);
@@ -2289,7 +2343,7 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             issued = g + 1;
             if (++sk == spt) {
                 sk = 0;
-                t += static_cast<int>(gridDim.x);
+                t += ncl;
             }
         }
         if (*reinterpret_cast<volatile int*>(&bars->abort))
@@ -2307,7 +2361,7 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
         bool ok = true;
         for (int g = 0; g < total; ++g) {
             const int s = g % NS, b = g & 1;
-            const int n = P.nk - sk * BPS < BPS ? P.nk - sk * BPS : BPS;
+            const int n = kb_hi - (kb_lo + sk * BPS) < BPS ? kb_hi - (kb_lo + sk * BPS) : BPS;
             // the stage's data, and from the third stage on its accumulator buffer back from promotion
             bool r = true;
             if (lane == 0) {
@@ -2351,7 +2405,7 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             const int s = g % NS;
             if (!warp_wait(&bars->xfull[s], (g / NS) & 1, &bars->abort, kFaultSwpSplit))
                 break;
-            const int n = P.nk - sk * BPS < BPS ? P.nk - sk * BPS : BPS;
+            const int n = kb_hi - (kb_lo + sk * BPS) < BPS ? kb_hi - (kb_lo + sk * BPS) : BPS;
             uint8_t* st = smem + s * C::kStageBytes;
 #pragma unroll
             for (int u = 0; u < kPer; ++u) {
@@ -2389,13 +2443,15 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             Rl[i] = 0.0f;
         }
         int sk = 0;
-        int t = static_cast<int>(blockIdx.x);
+        int t = cid;
+        int tt = 0;  // tiles finished by this CTA
         for (int g = 0; g < total; ++g) {
             const int b = g & 1;
             if (warp == 4)
                 (void)lane0_wait(&bars->dfull[b], (g >> 1) & 1, &bars->abort, kFaultSwpPromote);
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * swp::kPromoters) : "memory");
-            if (*reinterpret_cast<volatile int*>(&bars->abort))
+            // one verdict for all promotion warps: a flag read by each warp after a
+            // plain barrier could change between their reads
+            if (bar_red_or(1, 32 * swp::kPromoters, *reinterpret_cast<volatile int*>(&bars->abort) != 0))
                 break;
             tc_fence_after();
             uint32_t v[C::kCols];
@@ -2415,8 +2471,66 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
             }
             if (++sk == spt) {
                 // tile finished: this thread holds column col of y for rows 0..M-1
+                // (with split K, the partial sums of its rank's K range)
                 const int64_t col = static_cast<int64_t>(t) * swp::kTileN + wq * 32 + lane;
-                if (col < P.N) {
+                bool store = true;
+                if constexpr (KS > 1) {
+                    const int owner = wq * KS / 4;              // the rank that owns this warp's 32 columns
+                    const int lw = wq - owner * (4 / KS);       // the warp's index among the owner's
+                    float* redbuf = reinterpret_cast<float*>(smem + NS * C::kStageBytes + 512);
+                    auto slot = [&](int p) { return redbuf + ((p * (4 / KS) + lw) * 32 + lane) * (2 * MP); };
+                    // a failed wait sets the abort flag and skips the rest of the tile;
+                    // the promotion warps leave the loop together at the next
+                    // chunk's barrier reduction
+                    if (owner != rank) {
+                        // the owner must have read this slot for the previous tile
+                        if (tt > 0 && !warp_wait_acquire_cluster(&bars->rs_done[wq], static_cast<uint32_t>(tt - 1) & 1u,
+                                                                 &bars->abort, kFaultSwpReduce)) {
+                            store = false;
+                        } else {
+                            const uint32_t dst = mapa_shared(slot(rank), static_cast<uint32_t>(owner));
+#pragma unroll
+                            for (int i = 0; i < MP; i += 4) {
+                                st_cluster_v4(dst + 4u * i, Rh[i], Rh[i + 1], Rh[i + 2], Rh[i + 3]);
+                                st_cluster_v4(dst + 4u * (MP + i), Rl[i], Rl[i + 1], Rl[i + 2], Rl[i + 3]);
+                            }
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive_release_cluster(
+                                    mapa_shared(&bars->rs_full[wq], static_cast<uint32_t>(owner)));
+                            store = false;
+                        }
+                    } else if (!warp_wait_acquire_cluster(&bars->rs_full[wq], static_cast<uint32_t>(tt) & 1u, &bars->abort,
+                                                          kFaultSwpReduce)) {
+                        store = false;
+                    } else {
+                        // rank order: ranks 0 .. KS-1, this rank's own sums in its place
+                        float h[MP], l[MP];
+#pragma unroll
+                        for (int p = 0; p < KS; ++p) {
+                            const float* src = slot(p);
+#pragma unroll
+                            for (int i = 0; i < MP; ++i) {
+                                const float vh = p == rank ? Rh[i] : src[i];
+                                const float vl = p == rank ? Rl[i] : src[MP + i];
+                                h[i] = p == 0 ? vh : __fadd_rn(h[i], vh);
+                                l[i] = p == 0 ? vl : __fadd_rn(l[i], vl);
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < MP; ++i) {
+                            Rh[i] = h[i];
+                            Rl[i] = l[i];
+                        }
+                        __syncwarp();
+                        if (lane == 0)
+                            for (int p = 0; p < KS; ++p)
+                                if (p != rank)
+                                    mbar_arrive_release_cluster(mapa_shared(&bars->rs_done[wq], static_cast<uint32_t>(p)));
+                    }
+                    ++tt;
+                }
+                if (store && col < P.N) {
 #pragma unroll
                     for (int m = 0; m < MP; ++m)
                         if (m < P.M)
@@ -2431,17 +2545,37 @@ __global__ void __launch_bounds__(swp::kThreads, 1)
                     Rl[i] = 0.0f;
                 }
                 sk = 0;
-                t += static_cast<int>(gridDim.x);
+                t += ncl;
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if (KS > 1)
+        cluster_sync();  // no CTA leaves while another may still write its buffer or arrive on its barriers
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
+}
+
+template <int MP, int BPS, int NS, bool FX, bool EPI>
+__global__ void __launch_bounds__(swp::kThreads, 1)
+    comp_f16x2_swap_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
+                           const __grid_constant__ CUtensorMap tmap_w, const Problem P)
+{
+    swap_kernel_body<MP, BPS, NS, FX, EPI, 1>(tmap_hi, tmap_lo, tmap_w, P);
+}
+
+// The swapped-operand kernel with K split over a cluster of KS CTAs per tile.
+template <int MP, int BPS, int NS, bool FX, bool EPI, int KS>
+__global__ void __cluster_dims__(KS, 1, 1) __launch_bounds__(swp::kThreads, 1)
+    comp_f16x2_swap_splitk_kernel(const __grid_constant__ CUtensorMap tmap_hi,
+                                  const __grid_constant__ CUtensorMap tmap_lo,
+                                  const __grid_constant__ CUtensorMap tmap_w, const Problem P)
+{
+    swap_kernel_body<MP, BPS, NS, FX, EPI, KS>(tmap_hi, tmap_lo, tmap_w, P);
 }
 
 // ---------------------------------------------------------------------------
@@ -2684,11 +2818,16 @@ comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, con
                               : launch_x2_splitk_t<BN, NS, CH, AR, KS, false>(th, tl, tw, P, dev, stream);
 }
 
-template <int MP, int BPS, int NS, bool FX, bool EPI>
+template <int MP, int BPS, int NS, bool FX, bool EPI, int KS>
 comp_status_t launch_swap_t(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                           const DeviceInfo& dev, cudaStream_t stream)
 {
-    using C = swp::Cfg<MP, BPS, NS, FX>;
+    using C = swp::Cfg<MP, BPS, NS, FX, KS>;
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, Problem);
+    if constexpr (KS == 1)
+        kern = comp_f16x2_swap_kernel<MP, BPS, NS, FX, EPI>;
+    else
+        kern = comp_f16x2_swap_splitk_kernel<MP, BPS, NS, FX, EPI, KS>;
     static std::mutex mu;
     static bool done[64] = {};
     {
@@ -2696,24 +2835,48 @@ comp_status_t launch_swap_t(const CUtensorMap& th, const CUtensorMap& tl, const 
         if (dev.device < 0 || dev.device >= 64)
             return COMP_ERR_CUDA;
         if (!done[dev.device]) {
-            if (cudaFuncSetAttribute(comp_f16x2_swap_kernel<MP, BPS, NS, FX, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(C::kSmem)) != cudaSuccess) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem)) !=
+                cudaSuccess) {
                 (void)cudaGetLastError();
                 return COMP_ERR_CUDA;
             }
             done[dev.device] = true;
         }
     }
-    const int grid = P.tiles_n < dev.sm_count ? P.tiles_n : dev.sm_count;
-    return launch_pdl(comp_f16x2_swap_kernel<MP, BPS, NS, FX, EPI>, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
+    const int clusters = dev.sm_count / KS;
+    const int grid = KS * (P.tiles_n < clusters ? P.tiles_n : clusters);
+    return launch_pdl(kern, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
+}
+
+// K split of the swapped kernel: clusters of 4 CTAs per tile when four times
+// the tiles fit one wave and K has at least 16 blocks (4 or more per rank),
+// of 2 at twice the tiles with at least 8 blocks, else none.  With few tiles
+// of W this puts several CTAs on each tile's stream of W.
+int swap_split_ks(int tiles, int nk, int sm_count)
+{
+    if (tiles * 4 <= sm_count && nk >= 16)
+        return 4;
+    if (tiles * 2 <= sm_count && nk >= 8)
+        return 2;
+    return 1;
 }
 
 template <int MP, int BPS, int NS, bool FX = false>
 comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                           const DeviceInfo& dev, cudaStream_t stream)
 {
-    return (P.bias || P.gate) ? launch_swap_t<MP, BPS, NS, FX, true>(th, tl, tw, P, dev, stream)
-                              : launch_swap_t<MP, BPS, NS, FX, false>(th, tl, tw, P, dev, stream);
+    const bool epi = P.bias || P.gate;
+    switch (swap_split_ks(P.tiles_n, P.nk, dev.sm_count)) {
+    case 4:
+        return epi ? launch_swap_t<MP, BPS, NS, FX, true, 4>(th, tl, tw, P, dev, stream)
+                   : launch_swap_t<MP, BPS, NS, FX, false, 4>(th, tl, tw, P, dev, stream);
+    case 2:
+        return epi ? launch_swap_t<MP, BPS, NS, FX, true, 2>(th, tl, tw, P, dev, stream)
+                   : launch_swap_t<MP, BPS, NS, FX, false, 2>(th, tl, tw, P, dev, stream);
+    default:
+        return epi ? launch_swap_t<MP, BPS, NS, FX, true, 1>(th, tl, tw, P, dev, stream)
+                   : launch_swap_t<MP, BPS, NS, FX, false, 1>(th, tl, tw, P, dev, stream);
+    }
 }
 
 template <int BN, int NS, int CH, int AR, bool EPI>
@@ -2921,12 +3084,11 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     P.gate = epi.gate;
     P.stall = stall ? 1 : 0;
     CUtensorMap th{}, tl{}, tw{};
-    // at most 32 rows and at least 32 tiles of 128 columns: operands swapped,
-    // W streams through full 128-row MMAs (one CTA per tile, each streaming
-    // about 40-50 GB/s of W); with few tiles and a long K the split-K path
-    // below puts more CTAs on W
+    // at most 32 rows: operands swapped, W streams through full 128-row MMAs,
+    // with K split over a cluster of 2 or 4 CTAs per tile when W has few tiles
+    // (each CTA streams about 40-50 GB/s of W)
     const int64_t t128 = (N + swp::kTileN - 1) / swp::kTileN;
-    if (variant == 3 || (variant == 0 && M <= 32 && t128 >= 32 && !swap_few_tiles_long_k(N, K))) {
+    if (variant == 3 || (variant == 0 && M <= 32)) {
         const uint32_t mp = M <= 16 ? 16u : 32u;
         P.tiles_m = 1;
         P.tiles_n = static_cast<int>(t128);
@@ -3046,33 +3208,24 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     return launch_x2_bn<96, 4, 2>(th, tl, tw, P, dev, stream);
 }
 
-bool swap_few_tiles_long_k(int64_t N, int64_t K)
+bool swap_two_pass_better(int64_t M, int64_t N, int64_t K, int sm_count)
 {
-    // measured on GB300 (cold, L2 flushed): 16 x 4096 x 14336 took 69.6 us
-    // swapped against 53.3 us with K split over clusters of 4; at
-    // 16 x 4096 x 4096 the swapped kernel wins (24.6 against 30.7 us)
-    return (N + swp::kTileN - 1) / swp::kTileN <= 40 && (K + BK - 1) / BK >= 96;
-}
-
-bool swap_two_pass_better(int64_t M, int64_t N, int64_t K)
-{
-    // given a workspace: with 17 to 32 rows the fused kernel holds three
-    // 64 KB stages against the two-pass swapped product's four (32 x 4096 x
-    // 4096: 36.9 us fused, 26.6 us product + 6.1 us split, cold); with few
-    // tiles and a long K the two-pass form splits K (above).  A short K stays
-    // on the one-launch kernel.
-    const bool short_k = (K + BK - 1) / BK <= 8;
-    return !short_k && (M > 16 || swap_few_tiles_long_k(N, K));
+    // given a workspace: with 17 to 32 rows and no split of K the one-launch
+    // kernel holds three 64 KB stages (x in FP32 beside W) against the
+    // two-pass swapped product's four (32 x 4096 x 4096 without the split:
+    // 36.9 us one launch, 26.6 us product + 6.1 us split, cold).  A short K
+    // stays on the one-launch kernel.
+    const int tiles = static_cast<int>((N + swp::kTileN - 1) / swp::kTileN);
+    const int nk = static_cast<int>((K + BK - 1) / BK);
+    return M > 16 && nk > 8 && swap_split_ks(tiles, nk, sm_count) == 1;
 }
 
 bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K)
 {
-    // W spans at least 32 tiles of 128 rows (the kernel streams W at the rate
-    // of the access pattern), or the K loop is at most 8 blocks of 64 (a short
-    // problem, where one launch beats the two-pass form's split and product)
-    const bool wide = (N + swp::kTileN - 1) / swp::kTileN >= 32;
-    const bool short_k = (K + BK - 1) / BK <= 8;
-    return M <= 32 && (wide || short_k) && K % 8 == 0 && aligned16(x) && aligned16(W);
+    // at most 32 rows: the swapped kernel with the split fused, K split over a
+    // cluster when W has few tiles (W streams through 128-row MMAs; one launch)
+    (void)N;
+    return M <= 32 && K % 8 == 0 && aligned16(x) && aligned16(W);
 }
 
 comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,

@@ -39,16 +39,12 @@ struct Epilogue {
 };
 
 // Fused split and swapped-operand product for at most 32 rows of x (K a
-// multiple of 8, x and W 16-byte aligned); preferred once N spans 32 tiles of
-// 128, or when K is at most 8 blocks of 64.
+// multiple of 8, x and W 16-byte aligned), with K split over a cluster when W
+// has few tiles of 128 rows.
 bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K);
-// At most 32 rows against W of at most 40 tiles of 128 rows with K of at least
-// 96 blocks of 64: the two-pass product splits K over clusters instead of
-// swapping operands.
-bool swap_few_tiles_long_k(int64_t N, int64_t K);
 // Given a workspace, whether the two-pass form beats the fused swapped kernel
-// for a shape that swap_fused_preferred accepts.
-bool swap_two_pass_better(int64_t M, int64_t N, int64_t K);
+// for a shape that swap_fused_preferred accepts (17 to 32 rows, no split of K).
+bool swap_two_pass_better(int64_t M, int64_t N, int64_t K, int sm_count);
 comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                 const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi = Epilogue{});
 // Fused split and product on CTA pairs (K a multiple of 8, x and W 16-byte

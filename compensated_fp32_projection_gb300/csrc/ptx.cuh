@@ -344,6 +344,21 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t count, bool v)
     return r != 0;
 }
 
+// The same with the OR of the predicates.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %2, 0;\n\t"
+        "bar.red.or.pred p, %1, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(v ? 1u : 0u), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
 // when the issuing thread's earlier pair MMAs have completed.
 __device__ __forceinline__ void umma_commit_pair_by(uint32_t leader, uint64_t* bar, uint16_t cta_mask)

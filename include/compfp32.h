@@ -117,11 +117,12 @@ comp_status_t comp_geglu_f32(const float* gate, const float* up, float* out, int
  *   tensor-core accumulations of hi(x)·W^T and lo(x)·W^T.
  *   x : [M, K] binary32 (input).   W : [N, K] binary16 (input).   y : [M, N] binary32 (output).
  * One kernel: x is split on the fly in shared memory, both products accumulate
- * in tensor memory, and the merge is the epilogue.  For at most 32 rows
- * against at least 32 * 128 rows of W, or with K at most 512 (K a multiple of
- * 8, x and W 16-byte aligned), the kernel swaps the operands (y^T = W x^T,
- * 128 rows of W per MMA) and splits each K block of x into shared memory as
- * it streams W.  For more
+ * in tensor memory, and the merge is the epilogue.  For at most 32 rows (K a
+ * multiple of 8, x and W 16-byte aligned), the kernel swaps the operands
+ * (y^T = W x^T, 128 rows of W per MMA) and splits each K block of x into
+ * shared memory as it streams W; when W has few tiles of 128 rows, K is split
+ * over a cluster of 2 or 4 CTAs per tile and their partial sums are added in
+ * rank order (reruns give identical bits).  For more
  * than 128 rows, once the output fills about one wave of 128 x 192 tiles (same
  * operand conditions), a cluster of two CTAs computes each 256-row tile with
  * one instruction stream for both SMs' tensor cores; x arrives in FP32 and is
@@ -185,8 +186,9 @@ comp_status_t comp_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const uint
  * (with K split over a cluster of 2 or 4 CTAs when the tiles are few; the
  * partial sums are added in rank order, so reruns give identical bits), 2 pairs of CTAs
  * (one cluster, both SMs' tensor cores driven by one instruction stream) per
- * 256-row tile, 3 operands swapped (y^T = W x^T with 128 rows of W per tile;
- * M <= 32 only), 4 one tensor-core chain per product over all of K (hi and lo
+ * 256-row tile, 3 operands swapped (y^T = W x^T with 128 rows of W per tile,
+ * K split over a cluster of 2 or 4 CTAs when the tiles are few; M <= 32
+ * only), 4 one tensor-core chain per product over all of K (hi and lo
  * in separate FP32 accumulators, merged once at the tile end; one CTA per
  * 128 x 128 tile).  Variant 4 exists to measure what the chunked promotion of
  * the other kernels buys (laya.cpp docs/vulkan.md, AMD accumulation
@@ -221,13 +223,12 @@ int64_t comp_gemm_workspace_bytes_mnk(int64_t M, int64_t N, int64_t K);
  * (COMP_ERR_INVALID_VALUE); its contents are overwritten.  The call enqueues
  * the two-pass form: comp_split_f32 of x into the workspace, then
  * comp_gemm_f16x2.
- *   - M <= 32 against at least 32 * 128 rows of W or with K <= 512, K a
- *     multiple of 8, x and W 16-byte aligned: the fused swapped-operand kernel
- *     of comp_gemm_f32x16 instead (one launch; faster there than split plus
- *     product); the workspace is unused.  Except, when the planes fit the
- *     workspace and K > 512: with 17 to 32 rows, or with W of at most
- *     40 * 128 rows and K >= 6081 (96 blocks of 64), the two-pass form below
- *     is faster and runs instead.
+ *   - M <= 32, K a multiple of 8, x and W 16-byte aligned: the fused
+ *     swapped-operand kernel of comp_gemm_f32x16 instead (one launch; as fast
+ *     as split plus product or faster); the workspace is unused.  Except with
+ *     17 to 32 rows, K > 512 and W too wide for a split of K (more than
+ *     sm_count / 2 tiles of 128 rows), when the planes fit the workspace: the
+ *     two-pass form below, whose product holds more stages in flight.
  *   - K a multiple of 8, W 16-byte aligned, workspace of at least
  *     comp_gemm_workspace_bytes(M, K): the planes [M, K] (hi, then lo) and
  *     the caller's W.

@@ -54,11 +54,14 @@ def test_timeout_is_reported_and_the_context_stays_usable(pkg, orc):
 
 
 PAIR_CODES = {0x701, 0x702, 0x703}
-SWAP_CODES = {0x801, 0x802, 0x803, 0x804}
+SWAP_CODES = {0x801, 0x802, 0x803, 0x804, 0x805}
 
 
-@pytest.mark.parametrize("variant,shape,codes", [(2, (256, 224, 128), PAIR_CODES), (3, (16, 4096, 128), SWAP_CODES)],
-                         ids=["pairs", "swapped"])
+# swapped-split: 32 tiles of W with 16 K blocks, K split over clusters of 4
+# (every rank's first stage is left out; the ranks meet at the cluster barrier)
+@pytest.mark.parametrize("variant,shape,codes", [(2, (256, 224, 128), PAIR_CODES), (3, (16, 4096, 128), SWAP_CODES),
+                                                 (3, (16, 4096, 1024), SWAP_CODES)],
+                         ids=["pairs", "swapped", "swapped-split"])
 def test_stalled_pipeline_aborts_and_reports(pkg, orc, variant, shape, codes):
     from compensated_fp32_projection_gb300 import _native, workloads
     from gemm_check import check_comp

@@ -212,9 +212,10 @@ def test_device_status_clean_after_gemms(pkg):
     assert st == 0 and where == 0
 
 
-# At most 32 rows: the split fused into the swapped-operand kernel (automatic
-# once W spans 32 tiles of 128 rows; variant 3 forces it).  Ragged N tails,
-# K below one 64-wide block, K not a multiple of 64, one and 32 rows.
+# At most 32 rows: the split fused into the swapped-operand kernel (the
+# automatic choice for at most 32 rows; variant 3 forces it), with K split over
+# a cluster when W has few tiles.  Ragged N tails, K below one 64-wide block,
+# K not a multiple of 64, one and 32 rows.
 SWAPPED = [(16, 14336, 4096), (1, 4096, 64), (17, 5000, 520), (32, 4100, 1032), (5, 4096, 8), (32, 8192, 200),
            (8, 384, 256), (3, 130, 72)]
 
@@ -228,9 +229,8 @@ def test_fused_swapped(pkg, orc, shape):
     y = pkg.comp_gemm_f32x16_variant(x.cuda(), W.cuda(), 3)
     e_gpu, e_cast = check_comp(y, x, W, orc)
     assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
-    if (N + 127) // 128 >= 32 or (K + 63) // 64 <= 8:  # the automatic choice is the same kernel
-        y0 = pkg.comp_gemm_f32x16(x.cuda(), W.cuda())
-        assert torch.equal(y0.view(torch.int32), y.view(torch.int32))
+    y0 = pkg.comp_gemm_f32x16(x.cuda(), W.cuda())  # the automatic choice is the same kernel
+    assert torch.equal(y0.view(torch.int32), y.view(torch.int32))
 
 
 @pytest.mark.parametrize("shape", [(16, 14336, 4096), (32, 4100, 1032), (7, 2048, 136)],

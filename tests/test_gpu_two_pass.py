@@ -348,14 +348,19 @@ def test_product_bit_exact_through_identity(pkg, orc, variant, M):
     assert np.array_equal(y.view(np.uint32), y_or.view(np.uint32)), int(np.sum(y.view(np.uint32) != y_or.view(np.uint32)))
 
 
-# At most 32 rows, given a workspace: 17 to 32 rows against a wide W, or few
-# tiles of W with a long K, run the two-pass form (split, then the swapped
-# product or K split over clusters) instead of the one-launch swapped kernel;
-# the result is the explicit split + product's, bit for bit, and the oracle's
-# within the gate.
-@pytest.mark.parametrize("shape", [(32, 4096, 4096), (24, 4100, 1032), (16, 4096, 14336), (8, 3000, 6208)],
-                         ids=lambda s: "x".join(map(str, s)))
-def test_ws_routes_decode_shapes_to_the_two_pass_form(pkg, orc, shape):
+# At most 32 rows: comp_gemm_f32x16_ws runs the swapped kernel with the split
+# fused, with K split over a cluster of 2 or 4 CTAs when W has few tiles
+# (8 x 4096 x 4096: 4; 16 x 8192 x 4096: 2; 5 x 1000 x 2056, ragged N: 4;
+# 32 x 4096 x 4096, 32-row operands: 4), or, with 17 to 32 rows and no split,
+# the split and the swapped product (24 x 14336 x 1032).  Both forms give the
+# bits of the explicit split + product (identical stages and chunks), and the
+# oracle's results within the gate.
+FEW_ROWS = [(8, 4096, 4096), (16, 8192, 4096), (5, 1000, 2056), (32, 4096, 4096), (24, 14336, 1032),
+            (16, 4096, 14336)]
+
+
+@pytest.mark.parametrize("shape", FEW_ROWS, ids=lambda s: "x".join(map(str, s)))
+def test_ws_few_rows_equals_split_and_product(pkg, orc, shape):
     from compensated_fp32_projection_gb300 import workloads
 
     M, N, K = shape
@@ -368,3 +373,18 @@ def test_ws_routes_decode_shapes_to_the_two_pass_form(pkg, orc, shape):
     r, c = sample_outputs(M, N)
     e_gpu, e_cast = check_comp(y, x, W, orc, r, c)
     assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
+
+
+@pytest.mark.parametrize("shape", [(8, 4096, 4096), (16, 8192, 4096), (5, 1000, 2056)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_swapped_split_k_deterministic(pkg, shape):
+    # the swapped kernel with K split over a cluster adds the ranks' partial
+    # sums in rank order: bit-identical reruns
+    from compensated_fp32_projection_gb300 import workloads
+
+    M, N, K = shape
+    x, W = workloads.random_case(M, N, K, seed=5)
+    hi, lo = pkg.comp_split_f32(x.cuda())
+    y1 = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), 3)
+    y2 = pkg.comp_gemm_f16x2_variant(hi, lo, W.cuda(), 3)
+    assert torch.equal(bits(y1), bits(y2))
