@@ -132,7 +132,7 @@ comp_status_t gemm_ws_impl(const float* x, const uint16_t* W, float* y, int64_t 
     // at most 32 rows: one kernel with the split fused needs no workspace and
     // is as fast as the two-pass form or faster, except with 17 to 32 rows and
     // no split of K
-    if (swap_fused_preferred(x, W, M, N, K) && !(planes_fit && swap_two_pass_better(M, N, K, dev.sm_count)))
+    if (swap_fused_preferred(x, W, M, N, K) && !(planes_fit && swap_two_pass_better(M, N, K, dev)))
         return launch_swap_fused(x, W, y, M, N, K, dev, s, epi);
     // two-pass form on the caller's W: planes [M, K] in the workspace
     if (planes_fit) {

@@ -1205,9 +1205,11 @@ __device__ __forceinline__ void f16x2_tile_body(const CUtensorMap& tmap_hi, cons
                 }
             }
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0) {
+                fence_release_smem_cta_cluster();  // the reads of the receive buffer, before the senders reuse it
                 for (int p = 0; p < KS; ++p)
-                    mbar_arrive_release_cluster(mapa_shared(&bars->rs_done, static_cast<uint32_t>(p)));
+                    mbar_arrive_relaxed_cluster(mapa_shared(&bars->rs_done, static_cast<uint32_t>(p)));
+            }
             return true;
         };
         int g = 0, c = 0, kb = 0;
@@ -2479,6 +2481,10 @@ __device__ __forceinline__ void swap_kernel_body(const CUtensorMap& tmap_hi, con
                     const int lw = wq - owner * (4 / KS);       // the warp's index among the owner's
                     float* redbuf = reinterpret_cast<float*>(smem + NS * C::kStageBytes + 512);
                     auto slot = [&](int p) { return redbuf + ((p * (4 / KS) + lw) * 32 + lane) * (2 * MP); };
+                    // float offset of value v (a multiple of 4) in a lane's slot: the
+                    // 16-byte chunks rotated by lane, so that eight lanes' 16-byte
+                    // accesses at the same offset fall in eight different bank groups
+                    auto SW = [&](int v) { return ((v >> 2) ^ (lane & 7)) << 2; };
                     // a failed wait sets the abort flag and skips the rest of the tile;
                     // the promotion warps leave the loop together at the next
                     // chunk's barrier reduction
@@ -2491,8 +2497,8 @@ __device__ __forceinline__ void swap_kernel_body(const CUtensorMap& tmap_hi, con
                             const uint32_t dst = mapa_shared(slot(rank), static_cast<uint32_t>(owner));
 #pragma unroll
                             for (int i = 0; i < MP; i += 4) {
-                                st_cluster_v4(dst + 4u * i, Rh[i], Rh[i + 1], Rh[i + 2], Rh[i + 3]);
-                                st_cluster_v4(dst + 4u * (MP + i), Rl[i], Rl[i + 1], Rl[i + 2], Rl[i + 3]);
+                                st_cluster_v4(dst + 4u * SW(i), Rh[i], Rh[i + 1], Rh[i + 2], Rh[i + 3]);
+                                st_cluster_v4(dst + 4u * SW(MP + i), Rl[i], Rl[i + 1], Rl[i + 2], Rl[i + 3]);
                             }
                             __syncwarp();
                             if (lane == 0)
@@ -2504,29 +2510,46 @@ __device__ __forceinline__ void swap_kernel_body(const CUtensorMap& tmap_hi, con
                                                           kFaultSwpReduce)) {
                         store = false;
                     } else {
-                        // rank order: ranks 0 .. KS-1, this rank's own sums in its place
-                        float h[MP], l[MP];
+                        // rank order, ranks 0 .. KS-1: this rank's own sums go to its
+                        // own slot, then one pass adds the KS slots starting from -0
+                        // (-0 + v == v for every v, so the first addition is exact)
+                        {
+                            float* own = slot(rank);
 #pragma unroll
-                        for (int p = 0; p < KS; ++p) {
-                            const float* src = slot(p);
-#pragma unroll
-                            for (int i = 0; i < MP; ++i) {
-                                const float vh = p == rank ? Rh[i] : src[i];
-                                const float vl = p == rank ? Rl[i] : src[MP + i];
-                                h[i] = p == 0 ? vh : __fadd_rn(h[i], vh);
-                                l[i] = p == 0 ? vl : __fadd_rn(l[i], vl);
+                            for (int i = 0; i < MP; i += 4) {
+                                st_shared_v4(own + SW(i), Rh[i], Rh[i + 1], Rh[i + 2], Rh[i + 3]);
+                                st_shared_v4(own + SW(MP + i), Rl[i], Rl[i + 1], Rl[i + 2], Rl[i + 3]);
                             }
                         }
 #pragma unroll
                         for (int i = 0; i < MP; ++i) {
-                            Rh[i] = h[i];
-                            Rl[i] = l[i];
+                            Rh[i] = -0.0f;
+                            Rl[i] = -0.0f;
+                        }
+#pragma unroll 1
+                        for (int p = 0; p < KS; ++p) {
+                            const float* src = slot(p);
+#pragma unroll
+                            for (int i = 0; i < MP; i += 4) {
+                                const float4 a = *reinterpret_cast<const float4*>(src + SW(i));
+                                const float4 c = *reinterpret_cast<const float4*>(src + SW(MP + i));
+                                Rh[i] = __fadd_rn(Rh[i], a.x);
+                                Rh[i + 1] = __fadd_rn(Rh[i + 1], a.y);
+                                Rh[i + 2] = __fadd_rn(Rh[i + 2], a.z);
+                                Rh[i + 3] = __fadd_rn(Rh[i + 3], a.w);
+                                Rl[i] = __fadd_rn(Rl[i], c.x);
+                                Rl[i + 1] = __fadd_rn(Rl[i + 1], c.y);
+                                Rl[i + 2] = __fadd_rn(Rl[i + 2], c.z);
+                                Rl[i + 3] = __fadd_rn(Rl[i + 3], c.w);
+                            }
                         }
                         __syncwarp();
-                        if (lane == 0)
+                        if (lane == 0) {
+                            fence_release_smem_cta_cluster();  // the slots' reads, before the senders reuse them
                             for (int p = 0; p < KS; ++p)
                                 if (p != rank)
-                                    mbar_arrive_release_cluster(mapa_shared(&bars->rs_done[wq], static_cast<uint32_t>(p)));
+                                    mbar_arrive_relaxed_cluster(mapa_shared(&bars->rs_done[wq], static_cast<uint32_t>(p)));
+                        }
                     }
                     ++tt;
                 }
@@ -2770,40 +2793,48 @@ comp_status_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t
     return COMP_OK;
 }
 
+// Clusters of KS CTAs of the split-K instance that run at once on the device
+// (the occupancy API's count: clusters must fit inside one GPC, so it can be
+// below sm_count / KS); the first call per device also sets the kernel's
+// shared-memory limit.  0 on a CUDA error.
+template <int BN, int NS, int CH, int AR, int KS, bool EPI>
+int x2_resident_clusters(const DeviceInfo& dev)
+{
+    using C = x2::Cfg<BN, NS, CH, AR, KS>;
+    static std::mutex mu;
+    static int clusters[64] = {};  // per device, 0 = not yet known
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 0 || dev.device >= 64)
+        return 0;
+    if (clusters[dev.device] == 0) {
+        if (cudaFuncSetAttribute(comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS, EPI>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count / KS * KS), 1, 1);
+        cfg.blockDim = dim3(x2::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::kSmem;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS, EPI>, &cfg) != cudaSuccess ||
+            n <= 0) {
+            (void)cudaGetLastError();
+            n = dev.sm_count / KS;
+        }
+        clusters[dev.device] = n;
+    }
+    return clusters[dev.device];
+}
+
 template <int BN, int NS, int CH, int AR, int KS, bool EPI>
 comp_status_t launch_x2_splitk_t(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
                                  const DeviceInfo& dev, cudaStream_t stream)
 {
     using C = x2::Cfg<BN, NS, CH, AR, KS>;
-    static std::mutex mu;
-    static int clusters[64] = {};  // co-resident clusters per device, 0 = not yet known
-    int nc;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev.device < 0 || dev.device >= 64)
-            return COMP_ERR_CUDA;
-        if (clusters[dev.device] == 0) {
-            if (cudaFuncSetAttribute(comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS, EPI>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(C::kSmem)) != cudaSuccess) {
-                (void)cudaGetLastError();
-                return COMP_ERR_CUDA;
-            }
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count / KS * KS), 1, 1);
-            cfg.blockDim = dim3(x2::kThreads, 1, 1);
-            cfg.dynamicSmemBytes = C::kSmem;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS, EPI>, &cfg) !=
-                    cudaSuccess ||
-                n <= 0) {
-                (void)cudaGetLastError();
-                n = dev.sm_count / KS;
-            }
-            clusters[dev.device] = n;
-        }
-        nc = clusters[dev.device];
-    }
+    const int nc = x2_resident_clusters<BN, NS, CH, AR, KS, EPI>(dev);
+    if (nc <= 0)
+        return COMP_ERR_CUDA;
     const int tiles = P.tiles_m * P.tiles_n;
     const int grid = KS * (tiles < nc ? tiles : nc);
     return launch_pdl(comp_f16x2_splitk_kernel<BN, NS, CH, AR, KS, EPI>, grid, x2::kThreads, C::kSmem, stream, th, tl, tw,
@@ -2819,46 +2850,90 @@ comp_status_t launch_x2_splitk(const CUtensorMap& th, const CUtensorMap& tl, con
 }
 
 template <int MP, int BPS, int NS, bool FX, bool EPI, int KS>
-comp_status_t launch_swap_t(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
-                          const DeviceInfo& dev, cudaStream_t stream)
+auto swap_kernel_of()
 {
-    using C = swp::Cfg<MP, BPS, NS, FX, KS>;
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, Problem);
     if constexpr (KS == 1)
         kern = comp_f16x2_swap_kernel<MP, BPS, NS, FX, EPI>;
     else
         kern = comp_f16x2_swap_splitk_kernel<MP, BPS, NS, FX, EPI, KS>;
-    static std::mutex mu;
-    static bool done[64] = {};
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev.device < 0 || dev.device >= 64)
-            return COMP_ERR_CUDA;
-        if (!done[dev.device]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem)) !=
-                cudaSuccess) {
-                (void)cudaGetLastError();
-                return COMP_ERR_CUDA;
-            }
-            done[dev.device] = true;
-        }
-    }
-    const int clusters = dev.sm_count / KS;
-    const int grid = KS * (P.tiles_n < clusters ? P.tiles_n : clusters);
-    return launch_pdl(kern, grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
+    return kern;
 }
 
-// K split of the swapped kernel: clusters of 4 CTAs per tile when four times
-// the tiles fit one wave and K has at least 16 blocks (4 or more per rank),
-// of 2 at twice the tiles with at least 8 blocks, else none.  With few tiles
-// of W this puts several CTAs on each tile's stream of W.
-int swap_split_ks(int tiles, int nk, int sm_count)
+// Units of the swapped kernel instance that run at once on the device: CTAs
+// for KS = 1 (one per SM), else clusters of KS CTAs as the occupancy API
+// counts them.  Clusters must fit inside one GPC, so fewer than sm_count / KS
+// may be resident (36 clusters of 4 on a 152-SM GB300, not 38); a grid sized
+// past that runs its last clusters as a second wave.  The first call per
+// device also sets the kernel's shared-memory limit.  0 on a CUDA error.
+template <int MP, int BPS, int NS, bool FX, bool EPI, int KS>
+int swap_resident_units(const DeviceInfo& dev)
 {
-    if (tiles * 4 <= sm_count && nk >= 16)
+    using C = swp::Cfg<MP, BPS, NS, FX, KS>;
+    static std::mutex mu;
+    static int units[64] = {};  // per device, 0 = not yet known
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 0 || dev.device >= 64)
+        return 0;
+    if (units[dev.device] == 0) {
+        const auto kern = swap_kernel_of<MP, BPS, NS, FX, EPI, KS>();
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem)) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        int n = dev.sm_count / KS;
+        if (KS > 1) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count / KS * KS), 1, 1);
+            cfg.blockDim = dim3(swp::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = C::kSmem;
+            int q = 0;
+            if (cudaOccupancyMaxActiveClusters(&q, kern, &cfg) == cudaSuccess && q > 0)
+                n = q < n ? q : n;
+            else
+                (void)cudaGetLastError();
+        }
+        units[dev.device] = n;
+    }
+    return units[dev.device];
+}
+
+template <int MP, int BPS, int NS, bool FX, bool EPI, int KS>
+comp_status_t launch_swap_t(const CUtensorMap& th, const CUtensorMap& tl, const CUtensorMap& tw, const Problem& P,
+                          const DeviceInfo& dev, cudaStream_t stream)
+{
+    using C = swp::Cfg<MP, BPS, NS, FX, KS>;
+    const int units = swap_resident_units<MP, BPS, NS, FX, EPI, KS>(dev);
+    if (units <= 0)
+        return COMP_ERR_CUDA;
+    const int grid = KS * (P.tiles_n < units ? P.tiles_n : units);
+    return launch_pdl(swap_kernel_of<MP, BPS, NS, FX, EPI, KS>(), grid, swp::kThreads, C::kSmem, stream, th, tl, tw, P);
+}
+
+// K split of the swapped kernel: clusters of 4 CTAs per tile when every tile
+// gets a resident cluster of 4 at once and K has at least 16 blocks (4 or more
+// per rank), of 2 likewise with at least 8 blocks, else none.  With few tiles
+// of W this puts several CTAs on each tile's stream of W.  Several rounds of
+// split tiles do not pay: with 144 CTAs in clusters of 4 each CTA's stream of
+// W slowed to about half the rate of one CTA per tile.
+int swap_split_ks(int tiles, int nk, int clusters2, int clusters4)
+{
+    if (tiles <= clusters4 && nk >= 16)
         return 4;
-    if (tiles * 2 <= sm_count && nk >= 8)
+    if (tiles <= clusters2 && nk >= 8)
         return 2;
     return 1;
+}
+
+template <int MP, int BPS, int NS, bool FX>
+int swap_split_ks_for(const Problem& P, const DeviceInfo& dev, bool epi)
+{
+    const int c2 = epi ? swap_resident_units<MP, BPS, NS, FX, true, 2>(dev)
+                       : swap_resident_units<MP, BPS, NS, FX, false, 2>(dev);
+    const int c4 = epi ? swap_resident_units<MP, BPS, NS, FX, true, 4>(dev)
+                       : swap_resident_units<MP, BPS, NS, FX, false, 4>(dev);
+    return swap_split_ks(P.tiles_n, P.nk, c2, c4);
 }
 
 template <int MP, int BPS, int NS, bool FX = false>
@@ -2866,7 +2941,7 @@ comp_status_t launch_swap(const CUtensorMap& th, const CUtensorMap& tl, const CU
                           const DeviceInfo& dev, cudaStream_t stream)
 {
     const bool epi = P.bias || P.gate;
-    switch (swap_split_ks(P.tiles_n, P.nk, dev.sm_count)) {
+    switch (swap_split_ks_for<MP, BPS, NS, FX>(P, dev, epi)) {
     case 4:
         return epi ? launch_swap_t<MP, BPS, NS, FX, true, 4>(th, tl, tw, P, dev, stream)
                    : launch_swap_t<MP, BPS, NS, FX, false, 4>(th, tl, tw, P, dev, stream);
@@ -3139,14 +3214,15 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     }
     // few tiles: split K over clusters of 2 or 4 CTAs (at most 32 rows:
     // 192-wide tiles reduced in the leader; otherwise 128 x 128 tiles, or
-    // 128 x 64 tiles with a short K, reduced across the cluster)
+    // 128 x 64 tiles with a short K, reduced across the cluster), when every
+    // tile gets a resident cluster at once
     int ks = 1;
     bool narrow = false;  // 128 x 64 tiles
     if (M <= 32) {
         const int64_t t192 = (N + 191) / 192;
-        if (t192 * 4 <= dev.sm_count && P.nk >= 16)
+        if (t192 <= x2_resident_clusters<192, 6, 2, 32, 4, false>(dev) && P.nk >= 16)
             ks = 4;
-        else if (t192 * 2 <= dev.sm_count && P.nk >= 8)
+        else if (t192 <= x2_resident_clusters<192, 6, 2, 32, 2, false>(dev) && P.nk >= 8)
             ks = 2;
     } else {
         const int64_t t128 = ((M + BM - 1) / BM) * ((N + 127) / 128);
@@ -3160,7 +3236,7 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
             // 1000 x 776 x 1032 unsplit 20.5 / 15.1 against 22.5 / 17.3 split
             // over 2).  With a longer K the narrow MMAs lose (512 x 512 x 4096:
             // 30.7 against 28.7 us).
-            if (t64 * 2 <= dev.sm_count && P.nk >= 8) {
+            if (t64 <= x2_resident_clusters<64, 4, 2, BM, 2, false>(dev) && P.nk >= 8) {
                 ks = 2;
                 narrow = true;
             } else if (t64 <= dev.sm_count) {
@@ -3168,9 +3244,9 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
             }
         }
         if (!narrow) {
-            if (t128 * 4 <= dev.sm_count && P.nk >= 16)
+            if (t128 <= x2_resident_clusters<128, 3, 2, BM, 4, false>(dev) && P.nk >= 16)
                 ks = 4;
-            else if (t128 * 2 <= dev.sm_count && P.nk >= 8)
+            else if (t128 <= x2_resident_clusters<128, 3, 2, BM, 2, false>(dev) && P.nk >= 8)
                 ks = 2;
         }
     }
@@ -3208,7 +3284,7 @@ comp_status_t launch_gemm_f16x2(const uint16_t* hi, const uint16_t* lo, const ui
     return launch_x2_bn<96, 4, 2>(th, tl, tw, P, dev, stream);
 }
 
-bool swap_two_pass_better(int64_t M, int64_t N, int64_t K, int sm_count)
+bool swap_two_pass_better(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev)
 {
     // given a workspace: with 17 to 32 rows and no split of K the one-launch
     // kernel holds three 64 KB stages (x in FP32 beside W) against the
@@ -3217,7 +3293,13 @@ bool swap_two_pass_better(int64_t M, int64_t N, int64_t K, int sm_count)
     // stays on the one-launch kernel.
     const int tiles = static_cast<int>((N + swp::kTileN - 1) / swp::kTileN);
     const int nk = static_cast<int>((K + BK - 1) / BK);
-    return M > 16 && nk > 8 && swap_split_ks(tiles, nk, sm_count) == 1;
+    if (M <= 16 || nk <= 8)
+        return false;
+    // the fused kernel for 17 to 32 rows (launch_swap_fused's instance)
+    Problem P;
+    P.tiles_n = tiles;
+    P.nk = nk;
+    return swap_split_ks_for<32, 2, 3, true>(P, dev, false) == 1;
 }
 
 bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K)

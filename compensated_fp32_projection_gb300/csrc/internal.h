@@ -44,7 +44,7 @@ struct Epilogue {
 bool swap_fused_preferred(const float* x, const uint16_t* W, int64_t M, int64_t N, int64_t K);
 // Given a workspace, whether the two-pass form beats the fused swapped kernel
 // for a shape that swap_fused_preferred accepts (17 to 32 rows, no split of K).
-bool swap_two_pass_better(int64_t M, int64_t N, int64_t K, int sm_count);
+bool swap_two_pass_better(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 comp_status_t launch_swap_fused(const float* x, const uint16_t* W, float* y, int64_t M, int64_t N, int64_t K,
                                 const DeviceInfo& dev, cudaStream_t stream, const Epilogue& epi = Epilogue{});
 // Fused split and product on CTA pairs (K a multiple of 8, x and W 16-byte

@@ -466,6 +466,18 @@ __device__ __forceinline__ void mbar_arrive_release_smem_cluster(uint32_t cluste
         : "memory");
 }
 
+// The release fence of mbar_arrive_release_smem_cluster alone, and the
+// relaxed arrival alone: one fence, then arrivals on several CTAs' barriers.
+__device__ __forceinline__ void fence_release_smem_cta_cluster()
+{
+    asm volatile("fence.release.sync_restrict::shared::cta.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_relaxed_cluster(uint64_t* bar, uint32_t parity)
 {
     uint32_t ok;

@@ -226,8 +226,9 @@ int64_t comp_gemm_workspace_bytes_mnk(int64_t M, int64_t N, int64_t K);
  *   - M <= 32, K a multiple of 8, x and W 16-byte aligned: the fused
  *     swapped-operand kernel of comp_gemm_f32x16 instead (one launch; as fast
  *     as split plus product or faster); the workspace is unused.  Except with
- *     17 to 32 rows, K > 512 and W too wide for a split of K (more than
- *     sm_count / 2 tiles of 128 rows), when the planes fit the workspace: the
+ *     17 to 32 rows, K > 512 and W too wide for a split of K (more tiles of
+ *     128 rows than clusters of 2 CTAs of that kernel the device runs at
+ *     once, at most sm_count / 2), when the planes fit the workspace: the
  *     two-pass form below, whose product holds more stages in flight.
  *   - K a multiple of 8, W 16-byte aligned, workspace of at least
  *     comp_gemm_workspace_bytes(M, K): the planes [M, K] (hi, then lo) and

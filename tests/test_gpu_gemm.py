@@ -215,9 +215,11 @@ def test_device_status_clean_after_gemms(pkg):
 # At most 32 rows: the split fused into the swapped-operand kernel (the
 # automatic choice for at most 32 rows; variant 3 forces it), with K split over
 # a cluster when W has few tiles.  Ragged N tails, K below one 64-wide block,
-# K not a multiple of 64, one and 32 rows.
+# K not a multiple of 64, one and 32 rows.  36 and 38 tiles of W sit on either
+# side of the clusters of 4 that a 152-SM GB300 holds at once (36): clusters of
+# 4 for the first, pairs for the second.
 SWAPPED = [(16, 14336, 4096), (1, 4096, 64), (17, 5000, 520), (32, 4100, 1032), (5, 4096, 8), (32, 8192, 200),
-           (8, 384, 256), (3, 130, 72)]
+           (8, 384, 256), (3, 130, 72), (16, 4608, 1024), (8, 4864, 1024)]
 
 
 @pytest.mark.parametrize("shape", SWAPPED, ids=lambda s: "x".join(map(str, s)))

@@ -260,9 +260,12 @@ def test_device_status_clean(pkg):
 # (17, 260, 4096): clusters of 4.  128-row tiles with K split over a cluster
 # and the tile reduced across it (reduce-scatter): (512, 1024, 1024) and
 # (129, 257, 4096), ragged, clusters of 4; (300, 500, 520) and
-# (1000, 776, 1032), clusters of 2 (9 and 17 K blocks: uneven ranges)
+# (1000, 776, 1032), clusters of 2 (9 and 17 K blocks: uneven ranges).
+# (256, 2304, 2112) and (256, 2432, 2112): 36 and 38 tiles of 128 x 128, on
+# either side of the clusters of 4 that a 152-SM GB300 holds at once (36):
+# clusters of 4 for the first, of 2 for the second.
 SPLIT_K = [(16, 8000, 1024), (32, 1000, 520), (32, 2048, 2048), (512, 1024, 1024), (129, 257, 4096),
-           (300, 500, 520), (1000, 776, 1032)]
+           (300, 500, 520), (1000, 776, 1032), (256, 2304, 2112), (256, 2432, 2112)]
 
 
 @pytest.mark.parametrize("shape", SHAPES + SPLIT_K + [(2048, 2048, 256), (2000, 2001, 136), (300, 4096, 64)],
@@ -375,7 +378,8 @@ def test_ws_few_rows_equals_split_and_product(pkg, orc, shape):
     assert e_cast >= 100 * e_gpu, (e_cast, e_gpu)
 
 
-@pytest.mark.parametrize("shape", [(8, 4096, 4096), (16, 8192, 4096), (5, 1000, 2056)],
+@pytest.mark.parametrize("shape", [(8, 4096, 4096), (16, 8192, 4096), (5, 1000, 2056), (16, 4608, 1024),
+                                   (8, 4864, 1024)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_swapped_split_k_deterministic(pkg, shape):
     # the swapped kernel with K split over a cluster adds the ranks' partial
