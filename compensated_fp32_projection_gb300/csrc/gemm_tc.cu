@@ -2253,10 +2253,10 @@ __device__ __forceinline__ bool warp_wait_acquire_cluster(uint64_t* bar, uint32_
 // contiguous ranges of the K blocks; at the tile end rank r owns the tile's
 // columns 128 r / KS .. 128 (r + 1) / KS - 1: the other ranks' promotion warps
 // store their partial hi and lo sums of those columns into its receive buffer
-// (distributed shared memory) and arrive on its barrier with release at
-// cluster scope; the owner adds the KS partial sums in rank order (binary32,
-// round to nearest even), so reruns give identical bits, then merges and
-// stores y, and gives each slot back.
+// (distributed shared memory, st.async counting the bytes on its barrier,
+// which the owner arms with the bytes due); the owner adds the KS partial sums
+// in rank order (binary32, round to nearest even), so reruns give identical
+// bits, then merges and stores y, and gives each slot back.
 template <int MP, int BPS, int NS, bool FX, bool EPI, int KS>
 __device__ __forceinline__ void swap_kernel_body(const CUtensorMap& tmap_hi, const CUtensorMap& tmap_lo,
                                                  const CUtensorMap& tmap_w, const Problem& P)
@@ -2293,7 +2293,7 @@ __device__ __forceinline__ void swap_kernel_body(const CUtensorMap& tmap_hi, con
         }
         mbar_init(&bars->drain, 1);
         for (int w = 0; w < 4; ++w) {
-            mbar_init(&bars->rs_full[w], KS > 1 ? KS - 1 : 1);
+            mbar_init(&bars->rs_full[w], 1);  // the owner's expect_tx; the other ranks' bytes complete the phase
             mbar_init(&bars->rs_done[w], 1);
         }
         bars->abort = 0;
@@ -2488,22 +2488,23 @@ __device__ __forceinline__ void swap_kernel_body(const CUtensorMap& tmap_hi, con
                     // a failed wait sets the abort flag and skips the rest of the tile;
                     // the promotion warps leave the loop together at the next
                     // chunk's barrier reduction
+                    if (owner == rank && lane == 0)  // the other ranks' partial sums due this tile
+                        mbar_arrive_expect_tx(&bars->rs_full[wq], (KS - 1) * 32 * 2 * MP * 4);
                     if (owner != rank) {
                         // the owner must have read this slot for the previous tile
                         if (tt > 0 && !warp_wait_acquire_cluster(&bars->rs_done[wq], static_cast<uint32_t>(tt - 1) & 1u,
                                                                  &bars->abort, kFaultSwpReduce)) {
                             store = false;
                         } else {
+                            // asynchronous stores that count their bytes on the owner's
+                            // barrier (no fence or arrival here)
                             const uint32_t dst = mapa_shared(slot(rank), static_cast<uint32_t>(owner));
+                            const uint32_t rbar = mapa_shared(&bars->rs_full[wq], static_cast<uint32_t>(owner));
 #pragma unroll
                             for (int i = 0; i < MP; i += 4) {
-                                st_cluster_v4(dst + 4u * SW(i), Rh[i], Rh[i + 1], Rh[i + 2], Rh[i + 3]);
-                                st_cluster_v4(dst + 4u * SW(MP + i), Rl[i], Rl[i + 1], Rl[i + 2], Rl[i + 3]);
+                                st_async_v4(dst + 4u * SW(i), Rh[i], Rh[i + 1], Rh[i + 2], Rh[i + 3], rbar);
+                                st_async_v4(dst + 4u * SW(MP + i), Rl[i], Rl[i + 1], Rl[i + 2], Rl[i + 3], rbar);
                             }
-                            __syncwarp();
-                            if (lane == 0)
-                                mbar_arrive_release_cluster(
-                                    mapa_shared(&bars->rs_full[wq], static_cast<uint32_t>(owner)));
                             store = false;
                         }
                     } else if (!warp_wait_acquire_cluster(&bars->rs_full[wq], static_cast<uint32_t>(tt) & 1u, &bars->abort,

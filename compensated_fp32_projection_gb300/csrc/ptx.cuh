@@ -434,6 +434,19 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, fl
                  : "memory");
 }
 
+// Asynchronous 16-byte store into the shared memory of another CTA of the
+// cluster that counts its bytes on an mbarrier of that CTA (complete_tx): the
+// receiver arms the barrier with the bytes it expects and waits for the
+// phase; the sender needs no fence and no arrival.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
+                                            uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_addr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
